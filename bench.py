@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of single-token split-KV decode attention on GB300.
+
+A step is one decode step's attention over L layers of one geometry: every
+layer has its own Q and its own K/V cache, all resident in HBM, and the step
+runs the whole hot path (split kernel + merge kernel) once per layer. For the
+Gemma local sliding ring (the headline workload) L = 40, the sliding-window
+layers of Gemma 4 12B (48 layers, 8 of them global, per "Hand-Writing Gemma 4
+Flash-Decoding + an FP4 Matvec Bonus (Part 2)", section "The starting point",
+and mlxcel issue #683). The live-band bytes of all layers (tens to hundreds of
+MB) exceed the 129 MB L2, so no layer's K/V is still in L2 when it is read
+again one step later.
+
+Metric: live-band KV GB/s = sum over layers and sequences of
+band_b * NKV * HS * 2 (K and V) * 2 bytes, divided by the step time, and the
+same time as microseconds per layer. Device time comes from CUDA events around
+CUDA-graph replays of the step; e2e repeats the step through the public call
+(fd_decode_attn via the Python binding) with each step's queries and lengths
+copied from pinned host memory and the outputs copied back inside the timed
+region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+HEADLINE = "gemma_local_ring"
+METRIC = "decode-attn live-band KV GB/s (% of HBM peak) and µs/layer per geometry"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def live_band_bytes(w, lens) -> int:
+    keep = w.capacity if w.window <= 0 else min(w.window, w.capacity)
+    tot = 0
+    for L in lens.tolist():
+        L = max(0, int(L))
+        tot += L - max(0, L - keep)
+    return tot * w.NKV * w.HS * 2 * 2
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def layers_for(w, live, cap_layers=256):
+    """Enough layers that one step's live bytes exceed twice the L2, at least 4
+    (the headline ring uses its model's 40 layers)."""
+    if w.name == HEADLINE:
+        return 40
+    n = max(4, math.ceil(2 * L2_BYTES / max(1, live)))
+    alloc = 2 * w.B * w.NKV * w.capacity * w.HS * 2
+    n = min(n, cap_layers, max(2, (64 << 30) // alloc))
+    return n
+
+
+class Step:
+    """L layers of one geometry resident on the device."""
+
+    def __init__(self, w, layers, device, seed_base=0):
+        from decode_attention_04_gb300.inputs import draw_lens, make_inputs
+
+        self.w = w
+        self.L = layers
+        self.lens_h = draw_lens(w)
+        self.q, self.k, self.v = [], [], []
+        for i in range(layers):
+            q, k, v, _ = make_inputs(w, device=device, seed=w.seed * 1000 + seed_base + i, lens=self.lens_h)
+            self.q.append(q)
+            self.k.append(k)
+            self.v.append(v)
+        self.lens = self.lens_h.to(device)
+        self.out = [torch.empty_like(x) for x in self.q]
+        self.live = live_band_bytes(w, self.lens_h)
+
+    def run(self, stream=None):
+        import decode_attention_04_gb300 as fd
+        w = self.w
+        for i in range(self.L):
+            fd.fd_decode_attn(self.q[i], self.k[i], self.v[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
+                              w.capacity, w.window, w.scale, stream)
+
+
+def time_graph(step: Step, steps: int, warmup: int, stream):
+    """Capture the L-layer step in a CUDA graph; time `steps` replays with CUDA
+    events on the capture stream. Returns per-step milliseconds (list)."""
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            step.run(stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step.run(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            g.replay()
+    stream.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(steps):
+            g.replay()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)], g
+
+
+def time_e2e(step: Step, steps: int, warmup: int, stream):
+    """Each step: pinned host Q (all layers) and lens -> device, the L public
+    calls, outputs -> pinned host; CUDA events around the whole step."""
+    w = step.w
+    qh = torch.stack([x.cpu() for x in step.q]).pin_memory()
+    lh = step.lens_h.clone().pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    qd = torch.stack(step.q)  # staging on the device, one copy per step
+    saved_q, saved_out = step.q, step.out
+    step.q = list(qd.unbind(0))
+    od = torch.empty_like(qd)
+    step.out = list(od.unbind(0))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+
+    def one():
+        qd.copy_(qh, non_blocking=True)
+        step.lens.copy_(lh, non_blocking=True)
+        step.run(stream)
+        oh.copy_(od, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            one()
+        stream.synchronize()
+        ev[0].record(stream)
+        for i in range(steps):
+            one()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    step.q, step.out = saved_q, saved_out
+    ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    h2d = qh.numel() * qh.element_size() + lh.numel() * lh.element_size()
+    d2h = oh.numel() * oh.element_size()
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, step: Step, budget_s: float = 10.0):
+    """The FP64 oracle, as it stands, on this host's cores, over as many layers
+    of the step as fit in about `budget_s` seconds (at least one)."""
+    import oracle
+
+    oracle.build()
+    done, t_used, nbytes = 0, 0.0, 0
+    while done < step.L and t_used < budget_s:
+        q, k, v = step.q[done].cpu(), step.k[done].cpu(), step.v[done].cpu()
+        t0 = time.perf_counter()
+        oracle.decode(q, k, v, step.lens_h, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+        t_used += time.perf_counter() - t0
+        nbytes += step.live
+        done += 1
+    cores = os.cpu_count() or 1
+    return {"value": nbytes / t_used / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {step.L} layers of one step of {w.name} ({nbytes / 1e6:.1f} MB live band), "
+                      f"FP64, {cores} threads, {t_used:.2f} s"}
+
+
+def run_geometry(w, steps, warmup, stream, device, peak):
+    import decode_attention_04_gb300 as fd
+
+    from decode_attention_04_gb300.inputs import draw_lens
+    lens = draw_lens(w)
+    live = live_band_bytes(w, lens)
+    L = layers_for(w, live)
+    st = Step(w, L, device)
+    ms, _ = time_graph(st, steps, warmup, stream)
+    t = statistics.median(ms)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    gbs = st.live * L / (t * 1e-3) / 1e9
+    res = {"us_per_layer": t * 1e3 / L, "us_per_layer_min": min(ms) * 1e3 / L, "live_GBps": gbs,
+           "frac_of_peak": gbs / peak, "layers": L, "live_bytes_per_layer": st.live,
+           "num_splits": plan.num_splits, "desc": w.desc}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="fd", choices=["fd", "reference"])
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-geometries", action="store_true", help="skip the per-geometry table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from decode_attention_04_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return reference_arm(args, w, rank, world)
+
+    import decode_attention_04_gb300 as fd
+    from decode_attention_04_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(local)
+        dist.barrier()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    fd.load_library()
+    peak, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream(device)
+
+    step = Step(w, layers_for(w, 0), device)
+    L = step.L
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    kernels_per_call = 1 if plan.num_splits == 1 else 2
+
+    # ---- device-timed steps (graph replay), clocks sampled during the region
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms, graph = time_graph(step, args.steps, args.warmup, stream)
+    torch.cuda.synchronize()
+    tot_ms = sum(ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([tot_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+        tot_ms = t.item()
+    ms_per_step = tot_ms / args.steps
+    value = step.live * L * world / (ms_per_step * 1e-3) / 1e9
+    per_layer_us = ms_per_step * 1e3 / L
+    achieved = step.live / (per_layer_us * 1e-6) / 1e9
+
+    # ---- end to end through the public call, host buffers
+    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
+    e2e_value = step.live * L * world / (statistics.mean(e2e_ms) * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None if args.no_cpu_baseline else cpu_baseline(w, step)
+    live = step.live
+    del graph
+    clocks = clk.summary()
+    geoms = None
+    if not args.no_geometries:
+        del step
+        torch.cuda.empty_cache()
+        geoms = {}
+        for name, gw in WORKLOADS.items():
+            geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak)
+
+    traffic = None
+    tf = ROOT / "profiles" / "traffic.json"
+    if tf.exists():
+        try:
+            traffic = json.loads(tf.read_text()).get(w.name)
+        except (ValueError, OSError):
+            traffic = None
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "us_per_layer": per_layer_us,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: Q,K,V iid N(0,1) rounded to bf16, seeded",
+        "config": {
+            "workload": w.name,
+            "desc": w.desc,
+            "layers_per_step": L,
+            "live_band_bytes_per_layer": live,
+            "B": w.B, "NH": w.NH, "NKV": w.NKV, "HS": w.HS, "capacity": w.capacity, "window": w.window,
+            "num_splits": plan.num_splits,
+            "l2": f"inputs larger than L2: {L} layers x {live / 1e6:.1f} MB live band = {L * live / 1e6:.0f} MB per step vs 129 MB L2",
+            "timing": "CUDA events around CUDA-graph replays of the step, on the launching stream",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "one fd_decode_attn call (split kernel + merge kernel), averaged over the timed step",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+        },
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": args.steps * L * kernels_per_call,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "geometries": geoms,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def reference_arm(args, w, rank, world):
+    """--impl reference: the FP64 oracle as it stands on this host's cores, on
+    the same workload, metric and unit; each step is one layer of the step (a
+    bounded sample of the workload)."""
+    if rank != 0:
+        return 0
+    import oracle
+    from decode_attention_04_gb300.inputs import draw_lens, make_inputs
+
+    oracle.build()
+    lens = draw_lens(w)
+    live = live_band_bytes(w, lens)
+    q, k, v, _ = make_inputs(w, lens=lens)
+    for _ in range(args.warmup):
+        oracle.decode(q, k, v, lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(q, k, v, lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    dt = time.perf_counter() - t0
+    value = live * args.steps / dt / 1e9
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic: Q,K,V iid N(0,1) rounded to bf16, seeded",
+        "config": {"workload": w.name, "desc": w.desc, "layers_per_step": 1,
+                   "note": "each step is one layer of the fd step (bounded CPU sample)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} timed calls on one layer of {w.name}, FP64, {cores} threads"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

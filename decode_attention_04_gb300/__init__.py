@@ -1,0 +1,196 @@
+"""Python binding of libfd.so: single-token split-KV decode attention
+(Flash-Decoding) over a position-addressed bf16 KV cache on GB300.
+
+Every function here has the name of the C entry point it wraps
+(include/fd_decode_attn.h) and only marshals arguments: torch tensors become
+device pointers, the current torch stream becomes the CUDA stream, non-zero
+status codes become FdError. All arithmetic runs in libfd.so's kernels. There
+is no fallback: if libfd.so is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libfd.so"
+
+FD_OK = 0
+FD_ERR_INVALID_ARG = 1
+FD_ERR_UNSUPPORTED = 2
+FD_ERR_ALIGNMENT = 3
+FD_ERR_CUDA = 4
+FD_ERR_WORKSPACE = 5
+
+FD_DEVERR_LEN_NEGATIVE = 1 << 0
+FD_DEVERR_LEN_CLAMPED = 1 << 1
+FD_DEVERR_WAIT_TIMEOUT = 1 << 2
+
+FD_PATH_AUTO = 0
+FD_PATH_SIMT = 1
+FD_PATH_TC = 2
+
+EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_override", "fd_workspace_bytes", "fd_decode_attn",
+            "fd_decode_attn_ex", "fd_get_device_error", "fd_release", "fd_strerror", "fd_version"]
+
+
+class fd_plan_t(ctypes.Structure):
+    _fields_ = [
+        ("num_splits", ctypes.c_int),
+        ("path", ctypes.c_int),
+        ("granule", ctypes.c_int),
+        ("max_band", ctypes.c_int),
+        ("ctas_per_sm", ctypes.c_int),
+        ("num_sms", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("B", ctypes.c_int),
+        ("NH", ctypes.c_int),
+        ("NKV", ctypes.c_int),
+        ("HS", ctypes.c_int),
+        ("capacity", ctypes.c_int),
+        ("window", ctypes.c_int),
+    ]
+
+    def __repr__(self):
+        return "fd_plan_t(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+class FdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fd_strerror(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: Path | str | None = None):
+    """Load libfd.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = Path(path) if path else LIB_PATH
+    if not p.exists():
+        raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                           "(python -m decode_attention_04_gb300.build)")
+    lib = ctypes.CDLL(str(p))
+    ci, vp, sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    planp = ctypes.POINTER(fd_plan_t)
+    sig = {
+        "fd_plan": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, planp]),
+        "fd_plan_sms": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
+        "fd_plan_override": (ci, [planp, ci, ci]),
+        "fd_workspace_bytes": (sz, [planp]),
+        "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
+        "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                                   ctypes.c_float, vp]),
+        "fd_get_device_error": (ci, [vp, ctypes.POINTER(ctypes.c_uint)]),
+        "fd_release": (None, []),
+        "fd_strerror": (ctypes.c_char_p, [ci]),
+        "fd_version": (ci, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != FD_OK:
+        raise FdError(rc, where)
+
+
+def fd_strerror(status: int) -> str:
+    return load_library().fd_strerror(status).decode()
+
+
+def fd_version() -> int:
+    return load_library().fd_version()
+
+
+def fd_plan(B, NH, NKV, HS, capacity, window, max_len=0, device=None) -> fd_plan_t:
+    if device is None:
+        import torch
+        device = torch.cuda.current_device()
+    p = fd_plan_t()
+    _check(load_library().fd_plan(B, NH, NKV, HS, capacity, window, max_len, int(device), ctypes.byref(p)),
+           "fd_plan")
+    return p
+
+
+def fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm) -> fd_plan_t:
+    p = fd_plan_t()
+    _check(load_library().fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm,
+                                      ctypes.byref(p)), "fd_plan_sms")
+    return p
+
+
+def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO) -> fd_plan_t:
+    _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path), "fd_plan_override")
+    return plan
+
+
+def fd_workspace_bytes(plan: fd_plan_t) -> int:
+    return load_library().fd_workspace_bytes(ctypes.byref(plan))
+
+
+def fd_decode_attn(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale,
+                   stream=None) -> None:
+    _check(load_library().fd_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lens),
+                                         B, NH, NKV, HS, capacity, window, float(scale), _stream(stream)),
+           "fd_decode_attn")
+
+
+def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens,
+                      B, NH, NKV, HS, capacity, window, scale, stream=None) -> None:
+    _check(load_library().fd_decode_attn_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
+                                            _ptr(out_f32), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                            _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
+                                            _stream(stream)),
+           "fd_decode_attn_ex")
+
+
+def fd_get_device_error(stream=None) -> int:
+    err = ctypes.c_uint(0)
+    _check(load_library().fd_get_device_error(_stream(stream), ctypes.byref(err)), "fd_get_device_error")
+    return err.value
+
+
+def fd_release() -> None:
+    load_library().fd_release()
+
+
+def decode_attention(q, k_cache, v_cache, lens, window=0, scale=0.0, out=None, stream=None):
+    """Convenience form over torch tensors: q [B,NH,HS], caches [B,NKV,capacity,HS]
+    (bf16, CUDA), lens int32 [B] (CUDA). Allocates `out` if not given and calls
+    fd_decode_attn."""
+    import torch
+    B, NH, HS = q.shape
+    _, NKV, capacity, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    fd_decode_attn(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale, stream)
+    return out
+
+
+__all__ = EXPORTED + ["fd_plan_t", "FdError", "load_library", "decode_attention", "LIB_PATH"]

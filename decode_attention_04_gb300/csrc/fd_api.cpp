@@ -1,0 +1,313 @@
+// Host side of libfd.so: argument checks, the split plan, the library-owned
+// workspace, and the exported C entry points declared in fd_decode_attn.h.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "fd_decode_attn.h"
+#include "fd_internal.h"
+
+namespace {
+
+constexpr int kMaxGroup = 16;
+constexpr int kDefaultCtasPerSm = 2;
+
+bool supported_hs(int HS) { return HS == 64 || HS == 128 || HS == 256 || HS == 512; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int B, int NH, int NKV, int HS, int capacity, int window) {
+  if (B < 0 || NH <= 0 || NKV <= 0 || capacity <= 0) return FD_ERR_INVALID_ARG;
+  if (window > capacity) return FD_ERR_INVALID_ARG;
+  if (B > 65535 || NKV > 65535) return FD_ERR_INVALID_ARG;  // grid y/z limits
+  if (!supported_hs(HS)) return FD_ERR_UNSUPPORTED;
+  if (NH % NKV != 0 || NH / NKV > kMaxGroup) return FD_ERR_UNSUPPORTED;
+  return FD_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bytes of the (O) part of the workspace; the (m, l) part follows it.
+size_t ws_o_bytes(const fd_plan_t& p) {
+  return round_up(static_cast<size_t>(p.B) * p.NH * p.num_splits * p.HS * sizeof(float), 256);
+}
+
+size_t ws_total(const fd_plan_t& p) {
+  if (p.num_splits <= 1) return 0;
+  return ws_o_bytes(p) + round_up(static_cast<size_t>(p.B) * p.NH * p.num_splits * 2 * sizeof(float), 256);
+}
+
+// The split rule, documented in fd_decode_attn.h beside fd_plan_t.
+int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
+              int ctas_per_sm, int path, fd_plan_t* plan) {
+  if (!plan) return FD_ERR_INVALID_ARG;
+  int rc = check_shape(B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  if (num_sms <= 0 || ctas_per_sm <= 0) return FD_ERR_INVALID_ARG;
+  if (path == FD_PATH_AUTO) path = FD_PATH_TC;
+  if (path != FD_PATH_TC && path != FD_PATH_SIMT) return FD_ERR_INVALID_ARG;
+
+  const int keep = window > 0 ? window : capacity;
+  int max_band = keep < capacity ? keep : capacity;
+  if (max_len > 0 && max_len < max_band) max_band = max_len;
+  if (max_band < 1) max_band = 1;
+
+  const int granule = fd::plan_granule(path, HS);
+  const long long units = static_cast<long long>(B > 0 ? B : 1) * NKV;
+  const long long slots = static_cast<long long>(num_sms) * ctas_per_sm;
+  long long s_fill = (slots + units - 1) / units;
+  if (s_fill < 1) s_fill = 1;
+  auto chunk_for = [&](long long S) {
+    long long c = (max_band + S - 1) / S;
+    c = (c + granule - 1) / granule * granule;
+    return c < granule ? static_cast<long long>(granule) : c;
+  };
+  long long chunk = chunk_for(s_fill);
+  // Balance bound: at most ~2 MiB of K+V per split, so a ragged batch does not
+  // leave a few long splits running alone at the end.
+  const long long max_chunk = std::max<long long>(granule, (2ll << 20) / (4ll * HS));
+  long long S = (max_band + chunk - 1) / chunk;
+  if (chunk > max_chunk) {
+    long long waves = (static_cast<long long>(max_band) + max_chunk * s_fill - 1) / (max_chunk * s_fill);
+    S = waves * s_fill;
+    chunk = chunk_for(S);
+    S = (max_band + chunk - 1) / chunk;
+  }
+  if (S < 1) S = 1;
+  if (S > 65535 * 64) S = 65535 * 64;
+
+  fd_plan_t p{};
+  p.num_splits = static_cast<int>(S);
+  p.path = path;
+  p.granule = granule;
+  p.max_band = max_band;
+  p.ctas_per_sm = ctas_per_sm;
+  p.num_sms = num_sms;
+  p.B = B;
+  p.NH = NH;
+  p.NKV = NKV;
+  p.HS = HS;
+  p.capacity = capacity;
+  p.window = window;
+  p.workspace_bytes = ws_total(p);
+  *plan = p;
+  return FD_OK;
+}
+
+// Per-device SM count, cached.
+std::mutex g_mu;
+std::map<int, int> g_sms;
+
+int device_sms(int device, int* sms) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(device);
+    if (it != g_sms.end()) {
+      *sms = it->second;
+      return FD_OK;
+    }
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0)
+    return FD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_sms[device] = v;
+  *sms = v;
+  return FD_OK;
+}
+
+// Library-owned workspaces, one per (device, stream), grow-only.
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+int get_workspace(int device, cudaStream_t stream, size_t need, void** ptr) {
+  *ptr = nullptr;
+  if (need == 0) return FD_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[{device, reinterpret_cast<uintptr_t>(stream)}];
+  if (w.bytes >= need) {
+    *ptr = w.ptr;
+    return FD_OK;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FD_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return FD_ERR_WORKSPACE;
+  // The stream may still use the old buffer: finish its work before freeing.
+  if (w.ptr) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FD_ERR_CUDA;
+    cudaFree(w.ptr);
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, need) != cudaSuccess) return FD_ERR_CUDA;
+  w.ptr = p;
+  w.bytes = need;
+  *ptr = p;
+  return FD_OK;
+}
+
+int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* out_f32, const void* q,
+        const void* k_cache, const void* v_cache, void* out, const int* lens, float scale,
+        cudaStream_t stream) {
+  if (plan.B == 0) return FD_OK;
+  if (!q || !k_cache || !v_cache || !out || !lens) return FD_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(lens, 4) || (out_f32 && !aligned(out_f32, 16)))
+    return FD_ERR_ALIGNMENT;
+  const size_t need = ws_total(plan);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return FD_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return FD_ERR_ALIGNMENT;
+  }
+  if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(plan.HS));
+
+  fd::LaunchArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k_cache);
+  a.v = static_cast<const uint16_t*>(v_cache);
+  a.out = static_cast<uint16_t*>(out);
+  a.out_f32 = out_f32;
+  a.lens = lens;
+  a.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+  a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_o_bytes(plan)) : nullptr;
+  a.B = plan.B;
+  a.NH = plan.NH;
+  a.NKV = plan.NKV;
+  a.HS = plan.HS;
+  a.capacity = plan.capacity;
+  a.window = plan.window;
+  a.num_splits = plan.num_splits;
+  a.granule = plan.granule;
+  a.path = plan.path;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return fd::launch_decode(a, stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
+                int ctas_per_sm, fd_plan_t* plan) {
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, FD_PATH_AUTO, plan);
+}
+
+int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int device,
+            fd_plan_t* plan) {
+  if (!plan) return FD_ERR_INVALID_ARG;
+  int rc = check_shape(B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  int sms = 0;
+  rc = device_sms(device, &sms);
+  if (rc != FD_OK) return rc;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return FD_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return FD_ERR_CUDA;
+  int ctas = 0;
+  cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, NH / NKV, &ctas);
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess || ctas <= 0) return FD_ERR_CUDA;
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, FD_PATH_AUTO, plan);
+}
+
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path) {
+  if (!plan || num_splits < 0) return FD_ERR_INVALID_ARG;
+  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_TC) return FD_ERR_INVALID_ARG;
+  if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
+    return FD_ERR_INVALID_ARG;
+  if (path != FD_PATH_AUTO) {
+    plan->path = path;
+    plan->granule = fd::plan_granule(path, plan->HS);
+  }
+  if (num_splits > 0) {
+    if (num_splits > 65535 * 64) return FD_ERR_INVALID_ARG;
+    plan->num_splits = num_splits;
+  }
+  plan->workspace_bytes = ws_total(*plan);
+  return FD_OK;
+}
+
+size_t fd_workspace_bytes(const fd_plan_t* plan) { return plan ? ws_total(*plan) : 0; }
+
+int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes, float* out_f32,
+                      const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens,
+                      int B, int NH, int NKV, int HS, int capacity, int window, float scale,
+                      fd_stream_t stream) {
+  if (!plan) return FD_ERR_INVALID_ARG;
+  int rc = check_shape(B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  if (plan->B != B || plan->NH != NH || plan->NKV != NKV || plan->HS != HS || plan->capacity != capacity ||
+      plan->window != window)
+    return FD_ERR_INVALID_ARG;
+  if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1)
+    return FD_ERR_INVALID_ARG;
+  return run(*plan, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens, scale,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fd_decode_attn(const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens, int B,
+                   int NH, int NKV, int HS, int capacity, int window, float scale, fd_stream_t stream) {
+  int rc = check_shape(B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  if (B == 0) return FD_OK;
+  if (!q || !k_cache || !v_cache || !out || !lens) return FD_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return FD_ERR_CUDA;
+  fd_plan_t plan;
+  rc = fd_plan(B, NH, NKV, HS, capacity, window, 0, device, &plan);
+  if (rc != FD_OK) return rc;
+  void* ws = nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = get_workspace(device, s, plan.workspace_bytes, &ws);
+  if (rc != FD_OK) return rc;
+  return run(plan, ws, plan.workspace_bytes, nullptr, q, k_cache, v_cache, out, lens, scale, s);
+}
+
+int fd_get_device_error(fd_stream_t stream, unsigned int* err) {
+  if (!err) return FD_ERR_INVALID_ARG;
+  return fd::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), err) == cudaSuccess
+             ? FD_OK
+             : FD_ERR_CUDA;
+}
+
+void fd_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (auto& kv : g_ws) {
+    if (kv.second.ptr) {
+      int prev = 0;
+      cudaGetDevice(&prev);
+      cudaSetDevice(kv.first.first);
+      cudaFree(kv.second.ptr);
+      cudaSetDevice(prev);
+    }
+  }
+  g_ws.clear();
+}
+
+const char* fd_strerror(int status) {
+  switch (status) {
+    case FD_OK: return "ok";
+    case FD_ERR_INVALID_ARG: return "invalid argument";
+    case FD_ERR_UNSUPPORTED: return "unsupported shape (HS must be 64/128/256/512, NH % NKV == 0, NH/NKV <= 16)";
+    case FD_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for tensors and workspace, 4 for lens)";
+    case FD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case FD_ERR_WORKSPACE: return "workspace too small, or would need allocating while the stream is captured";
+    default: return "unknown status";
+  }
+}
+
+int fd_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+}  // extern "C"

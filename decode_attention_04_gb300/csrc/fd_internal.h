@@ -1,0 +1,44 @@
+// Internal interface between the host API (fd_api.cpp) and the kernels
+// (fd_kernels.cu). Not installed; the public interface is
+// include/fd_decode_attn.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace fd {
+
+// Everything a launch needs; filled and validated by the host API.
+struct LaunchArgs {
+  const uint16_t* q;        // bf16 [B][NH][HS]
+  const uint16_t* k;        // bf16 [B][NKV][capacity][HS]
+  const uint16_t* v;        // bf16 [B][NKV][capacity][HS]
+  uint16_t* out;            // bf16 [B][NH][HS]
+  float* out_f32;           // fp32 [B][NH][HS] or nullptr
+  const int* lens;          // int32 [B]
+  float* ws_o;              // fp32 [B][NH][S][HS]  (S > 1 only)
+  float* ws_ml;             // fp32 [B][NH][S][2]   (m in log2 units, l)
+  int B, NH, NKV, HS, capacity, window;  // window <= 0: none
+  int num_splits;           // S
+  int granule;              // chunk rounding, positions
+  int path;                 // FD_PATH_SIMT / FD_PATH_TC
+  float scale_log2;         // scale * log2(e)
+};
+
+// Positions per pipeline tile of the tensor-core kernel for head size HS, and
+// the chunk granule the plan uses for it.
+int tc_tile_positions(int HS);
+int plan_granule(int path, int HS);
+
+// Resident CTAs per SM of the kernel a plan would launch (occupancy query).
+cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas);
+
+// Launch the split kernel (and the merge kernel when S > 1) on `stream`.
+cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);
+
+// Read and clear the device error word of the current device.
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err);
+
+}  // namespace fd

@@ -1,0 +1,766 @@
+// Split-KV decode attention kernels for sm_103a (GB300).
+//
+// The method is the Flash-Decoding formulation of "Hand-Writing Gemma 4
+// Flash-Decoding + an FP4 Matvec Bonus (Part 2)", section "One KV head breaks
+// the textbook": every (sequence b, KV head, split s) thread block walks the
+// absolute positions of its slice of the live band [max(0, len - W), len),
+// reads position p from cache slot p % capacity, and leaves an unnormalised
+// (O, m, l) partial; a merge kernel combines the partials with the
+// online-softmax rule. Softmax state is rescaled once per tile of positions,
+// not once per position (same section, last bullet).
+//
+// Kernels:
+//   split_simt_kernel  per-position fp32 kernel; the plain reference GPU path.
+//   split_tc_kernel    the hot path: a producer warp streams K/V rows of the
+//                      band into a ring of shared-memory stages with 1-D bulk
+//                      async copies (cp.async.bulk + mbarrier transaction
+//                      counts); consumer warps compute the Q-group scores of a
+//                      tile with bf16 tensor-core MMAs (S^T = K Q^T, so the
+//                      positions fill the 16-row side and the G <= 16 query
+//                      rows the 8-wide side), rescale once per tile, and
+//                      accumulate O^T = V^T P^T on the tensor cores.
+//   merge_kernel       online-softmax merge of the S partials of each row.
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fd_decode_attn.h"
+#include "fd_internal.h"
+
+namespace fd {
+
+__device__ unsigned int g_device_error;
+
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Live band of sequence b: positions [lo, lo + band). Reports repaired
+// lengths through the device error word when `report` is set.
+__device__ __forceinline__ int band_of(int len, int capacity, int window, bool report, int* lo) {
+  unsigned flags = 0;
+  if (len < 0) {
+    flags |= FD_DEVERR_LEN_NEGATIVE;
+    len = 0;
+  }
+  int keep = capacity;
+  if (window > 0) {
+    keep = min(window, capacity);
+  } else if (len > capacity) {
+    flags |= FD_DEVERR_LEN_CLAMPED;
+  }
+  const int l0 = max(0, len - keep);
+  if (report && flags) atomicOr(&g_device_error, flags);
+  *lo = l0;
+  return len - l0;
+}
+
+// Positions per split for a band: ceil(band / S) rounded up to the granule.
+__device__ __forceinline__ int chunk_of(int band, int num_splits, int granule) {
+  const long long c = (static_cast<long long>(band) + num_splits - 1) / num_splits;
+  const long long r = ((c + granule - 1) / granule) * granule;
+  return static_cast<int>(r < granule ? granule : r);
+}
+
+__device__ __forceinline__ int active_splits(int band, int chunk) {
+  return band <= 0 ? 0 : (band + chunk - 1) / chunk;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after about one second of wall time, raises
+// FD_DEVERR_WAIT_TIMEOUT and returns false. `failed` is sticky per thread, so
+// after one timeout every later wait of that thread returns at once and the
+// kernel runs to its end; no wait in this library can hang the GPU.
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& failed) {
+  if (failed) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+  }
+  failed = true;
+  atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);
+  return false;
+}
+
+// 1-D bulk async copy global -> this CTA's shared memory, completing bytes on
+// the mbarrier. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A(16x16, row) * B(16x8, col), bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ======================================================= SIMT reference kernel
+
+constexpr int kSimtThreads = 128;
+
+// One block per (split, KV head, sequence). Each thread owns dims
+// tid, tid + 128, ... of every query row of the group; per position the G dot
+// products are reduced across the block, the online-softmax state is updated
+// for that single position, and O is rescaled. Shared memory: q [G][HS],
+// O [G][HS], per-warp partial dots [4][G], and per-row m, l, alpha, p.
+__global__ void __launch_bounds__(kSimtThreads) split_simt_kernel(const LaunchArgs a) {
+  extern __shared__ float sm[];
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = a.NH / a.NKV, HS = a.HS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* sq = sm;                    // [G][HS]
+  float* so = sq + G * HS;           // [G][HS]
+  float* sred = so + G * HS;         // [4][G]
+  float* sm_run = sred + 4 * G;      // [G]
+  float* sl_run = sm_run + G;        // [G]
+  float* salpha = sl_run + G;        // [G]
+  float* sp = salpha + G;            // [G]
+
+  int lo;
+  const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
+  const int chunk = chunk_of(band, a.num_splits, a.granule);
+  const long long p0 = lo + static_cast<long long>(s) * chunk;
+  const long long p1 = min(static_cast<long long>(lo) + band, p0 + chunk);
+  const bool direct = a.num_splits == 1;
+  const int hbase = kvh * G;
+
+  if (p0 >= p1) {
+    if (direct) {  // len == 0: the output row is zero
+      for (int i = tid; i < G * HS; i += kSimtThreads) {
+        const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / HS) * HS + i % HS;
+        a.out[o] = 0;
+        if (a.out_f32) a.out_f32[o] = 0.f;
+      }
+    }
+    return;
+  }
+
+  for (int i = tid; i < G * HS; i += kSimtThreads) {
+    sq[i] = bf16_bits_to_f32(a.q[(static_cast<size_t>(b) * a.NH + hbase) * HS + i]);
+    so[i] = 0.f;
+  }
+  if (tid < G) {
+    sm_run[tid] = kNegInf;
+    sl_run[tid] = 0.f;
+  }
+  __syncthreads();
+
+  const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
+  for (long long pos = p0; pos < p1; ++pos) {
+    const size_t row = (head_row0 + static_cast<size_t>(pos % a.capacity)) * HS;
+    for (int g = 0; g < G; ++g) {
+      float part = 0.f;
+      for (int d = tid; d < HS; d += kSimtThreads) part += sq[g * HS + d] * bf16_bits_to_f32(a.k[row + d]);
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      if (lane == 0) sred[warp * G + g] = part;
+    }
+    __syncthreads();
+    if (tid < G) {
+      float sc = 0.f;
+      for (int w = 0; w < kSimtThreads / 32; ++w) sc += sred[w * G + tid];
+      sc *= a.scale_log2;
+      const float m_old = sm_run[tid];
+      const float m_new = fmaxf(m_old, sc);
+      const float alpha = (m_new == kNegInf) ? 1.f : exp2f(m_old - m_new);
+      const float p = exp2f(sc - m_new);
+      sl_run[tid] = sl_run[tid] * alpha + p;
+      sm_run[tid] = isnan(sc) ? sc : m_new;
+      salpha[tid] = isnan(sc) ? sc : alpha;
+      sp[tid] = p;
+    }
+    __syncthreads();
+    for (int g = 0; g < G; ++g) {
+      const float al = salpha[g], p = sp[g];
+      for (int d = tid; d < HS; d += kSimtThreads)
+        so[g * HS + d] = so[g * HS + d] * al + p * bf16_bits_to_f32(a.v[row + d]);
+    }
+  }
+  __syncthreads();
+
+  for (int i = tid; i < G * HS; i += kSimtThreads) {
+    const int g = i / HS, d = i % HS;
+    const int h = hbase + g;
+    if (direct) {
+      const float val = so[i] / sl_run[g];
+      const size_t o = (static_cast<size_t>(b) * a.NH + h) * HS + d;
+      a.out[o] = f32_to_bf16_bits(val);
+      if (a.out_f32) a.out_f32[o] = val;
+    } else {
+      a.ws_o[((static_cast<size_t>(b) * a.NH + h) * a.num_splits + s) * HS + d] = so[i];
+    }
+  }
+  if (!direct && tid < G) {
+    const size_t r = ((static_cast<size_t>(b) * a.NH + hbase + tid) * a.num_splits + s) * 2;
+    a.ws_ml[r] = sm_run[tid];
+    a.ws_ml[r + 1] = sl_run[tid];
+  }
+}
+
+size_t simt_smem_bytes(int G, int HS) {
+  return (static_cast<size_t>(2) * G * HS + 4 * G + 4 * G) * sizeof(float);
+}
+
+// ===================================================== tensor-core split kernel
+
+template <int HS_, int NT_, int T_, int NWC_, int NSTAGE_>
+struct TcCfg {
+  static constexpr int HS = HS_;
+  static constexpr int NT = NT_;          // 8-row tiles of query rows (G <= 8 * NT)
+  static constexpr int NP = 8 * NT;       // padded query rows
+  static constexpr int T = T_;            // positions per pipeline tile
+  static constexpr int NWC = NWC_;        // consumer warps
+  static constexpr int NSTAGE = NSTAGE_;  // shared-memory ring depth
+  static constexpr int THREADS = (NWC + 1) * 32;
+  static constexpr int CTHREADS = NWC * 32;
+  static constexpr int PITCH = HS + 8;    // staged row pitch (bf16); +16 B keeps ldmatrix conflict-free
+  static constexpr int ROWB = HS * 2;     // bytes of one cache row
+  static constexpr int DW = HS / NWC;     // head dims owned by one consumer warp
+  static constexpr int KD = DW / 16;      // 16-dim steps per warp
+  static constexpr int MP = T / 16;       // 16-position tiles per pipeline tile
+  static constexpr int PPITCH = T + 8;    // P row pitch (bf16)
+  static constexpr int TPR = CTHREADS / NP;  // softmax threads per query row
+  static constexpr int PPT = T / TPR;        // positions per softmax thread
+  static constexpr size_t STAGE_BYTES = static_cast<size_t>(T) * PITCH * 2;
+  static constexpr size_t OFF_K = 0;
+  static constexpr size_t OFF_V = OFF_K + NSTAGE * STAGE_BYTES;
+  static constexpr size_t OFF_S = OFF_V + NSTAGE * STAGE_BYTES;              // f32 [NWC][T][NP]
+  static constexpr size_t OFF_P = OFF_S + static_cast<size_t>(NWC) * T * NP * 4;  // bf16 [2][NP][PPITCH]
+  static constexpr size_t OFF_A = OFF_P + static_cast<size_t>(2) * NP * PPITCH * 2;  // f32 alpha,m,l [NP]
+  static constexpr size_t OFF_BAR = (OFF_A + 3 * NP * 4 + 7) / 8 * 8;        // u64 full[], empty[]
+  static constexpr size_t SMEM = OFF_BAR + 2 * NSTAGE * 8;
+  static_assert(HS % (16 * NWC) == 0, "head dims must split into 16-wide slices per warp");
+  static_assert(T % 16 == 0 && T % TPR == 0, "tile must be whole 16-position MMA tiles");
+  static_assert(TPR <= 32 && 32 % TPR == 0, "a row's softmax threads must sit in one warp");
+  static_assert(ROWB % 16 == 0 && (PITCH * 2) % 16 == 0, "bulk copies need 16-byte rows");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = a.NH / a.NKV;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hbase = kvh * G;
+
+  int lo;
+  const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
+  const int chunk = chunk_of(band, a.num_splits, a.granule);
+  const long long p0 = lo + static_cast<long long>(s) * chunk;
+  const long long p1 = min(static_cast<long long>(lo) + band, p0 + chunk);
+  const bool direct = a.num_splits == 1;
+
+  if (p0 >= p1) {
+    if (direct) {  // len == 0: the output row is zero
+      for (int i = tid; i < G * C::HS; i += C::THREADS) {
+        const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / C::HS) * C::HS + i % C::HS;
+        a.out[o] = 0;
+        if (a.out_f32) a.out_f32[o] = 0.f;
+      }
+    }
+    return;
+  }
+  const int n = static_cast<int>(p1 - p0);
+  const int ntiles = (n + C::T - 1) / C::T;
+
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + C::OFF_K);
+  uint16_t* sV = reinterpret_cast<uint16_t*>(smem + C::OFF_V);
+  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
+  uint16_t* sP = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
+  float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
+  float* sM = sAlpha + C::NP;
+  float* sL = sM + C::NP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::NSTAGE);
+
+  if (tid == 0) {
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(full0 + 8 * i, 32);         // every producer lane arrives once per phase
+      mbar_init(empty0 + 8 * i, C::NWC);    // one arrival per consumer warp
+    }
+    fence_mbar_init();
+  }
+  // P rows beyond G are never written by the softmax; keep them zero. alpha of
+  // those rows stays 1 so their (discarded) accumulators stay finite.
+  for (int i = tid; i < 2 * C::NP * C::PPITCH; i += C::THREADS) sP[i] = 0;
+  for (int i = tid; i < C::NP; i += C::THREADS) {
+    sAlpha[i] = 1.f;
+    sM[i] = kNegInf;
+    sL[i] = 0.f;
+  }
+  __syncthreads();
+
+  if (warp == C::NWC) {
+    // ------------------------------------------------------------ producer
+    const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
+    const uint16_t* kb = a.k + head_row0 * C::HS;
+    const uint16_t* vb = a.v + head_row0 * C::HS;
+    bool failed = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % C::NSTAGE;
+      if (i >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((i / C::NSTAGE) - 1) & 1, failed);
+      const int nv = min(C::T, n - i * C::T);
+      const int mine = lane < nv ? (nv - lane + 31) / 32 : 0;
+      const uint32_t fb = full0 + 8 * st;
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mine) * 2u * C::ROWB);
+      const long long pbase = p0 + static_cast<long long>(i) * C::T;
+      const uint32_t dk = smem_u32(sK + static_cast<size_t>(st) * C::T * C::PITCH);
+      const uint32_t dv = smem_u32(sV + static_cast<size_t>(st) * C::T * C::PITCH);
+      for (int j = lane; j < nv; j += 32) {
+        const size_t slot = static_cast<size_t>((pbase + j) % a.capacity);
+        bulk_g2s(dk + j * C::PITCH * 2, kb + slot * C::HS, C::ROWB, fb);
+        bulk_g2s(dv + j * C::PITCH * 2, vb + slot * C::HS, C::ROWB, fb);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int grp = lane >> 2, t4 = lane & 3;
+  const int dbase = warp * C::DW;
+
+  // Q^T as MMA B fragments for this warp's dims: b0 = (dims 2t4..2t4+1, row grp),
+  // b1 = (dims 8+2t4.., row grp) of each 16-dim step.
+  uint32_t qf[C::KD][C::NT][2];
+#pragma unroll
+  for (int ks = 0; ks < C::KD; ++ks)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+      const int r = nt * 8 + grp;
+      uint32_t x0 = 0, x1 = 0;
+      if (r < G) {
+        const uint16_t* qr = a.q + (static_cast<size_t>(b) * a.NH + hbase + r) * C::HS + dbase + ks * 16 + 2 * t4;
+        x0 = *reinterpret_cast<const uint32_t*>(qr);
+        x1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+      }
+      qf[ks][nt][0] = x0;
+      qf[ks][nt][1] = x1;
+    }
+
+  float o[C::KD][C::NT][4];
+#pragma unroll
+  for (int mt = 0; mt < C::KD; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+
+  // softmax role: row sr, positions sj + TPR * t
+  const int sr = tid / C::TPR, sj = tid % C::TPR;
+  float m_run = kNegInf, l_run = 0.f;
+
+  // ldmatrix lane addressing
+  const int lrow = lane & 7, lmat = lane >> 3;
+  bool failed = false;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int st = i % C::NSTAGE;
+    mbar_wait(full0 + 8 * st, (i / C::NSTAGE) & 1, failed);
+    const int nv = min(C::T, n - i * C::T);
+    const int nv16 = (nv + 15) & ~15;
+    const uint16_t* tK = sK + static_cast<size_t>(st) * C::T * C::PITCH;
+    uint16_t* tV = sV + static_cast<size_t>(st) * C::T * C::PITCH;
+
+    // ---- scores: S^T[pos][row] partial over this warp's dims
+    float* myS = sS + static_cast<size_t>(warp) * C::T * C::NP;
+#pragma unroll
+    for (int mt = 0; mt < C::MP; ++mt) {
+      if (mt * 16 < nv) {
+        float acc[C::NT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::KD; ++ks) {
+          // matrices: (pos 0-7, d 0-7), (pos 8-15, d 0-7), (pos 0-7, d 8-15), (pos 8-15, d 8-15)
+          const int prow = mt * 16 + lrow + (lmat & 1) * 8;
+          const int dcol = dbase + ks * 16 + (lmat >> 1) * 8;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(smem_u32(tK + prow * C::PITCH + dcol), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          float* d0 = myS + (mt * 16 + grp) * C::NP + nt * 8 + 2 * t4;
+          *reinterpret_cast<float2*>(d0) = make_float2(acc[nt][0], acc[nt][1]);
+          *reinterpret_cast<float2*>(d0 + 8 * C::NP) = make_float2(acc[nt][2], acc[nt][3]);
+        }
+      }
+    }
+    named_bar_sync(1, C::CTHREADS);
+
+    // ---- one online-softmax update per row for the whole tile
+    if (sr < G) {
+      float sv[C::PPT];
+      float tmax = kNegInf;
+#pragma unroll
+      for (int t = 0; t < C::PPT; ++t) {
+        const int j = sj + t * C::TPR;
+        float x = kNegInf;
+        if (j < nv) {
+          float acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < C::NWC; ++w) acc += sS[(static_cast<size_t>(w) * C::T + j) * C::NP + sr];
+          x = acc * a.scale_log2;
+        }
+        sv[t] = x;
+        tmax = fmaxf(tmax, x);
+        if (isnan(x)) tmax = x;
+      }
+#pragma unroll
+      for (int off = C::TPR / 2; off > 0; off >>= 1) {
+        const float other = __shfl_xor_sync(0xffffffffu, tmax, off);
+        tmax = isnan(other) ? other : fmaxf(tmax, other);
+      }
+      const float m_new = isnan(tmax) ? tmax : fmaxf(m_run, tmax);
+      const float alpha = (m_new == kNegInf) ? 1.f : exp2f(m_run - m_new);
+      float psum = 0.f;
+      uint16_t* phi = sP + sr * C::PPITCH;
+      uint16_t* plo = sP + (C::NP + sr) * C::PPITCH;
+#pragma unroll
+      for (int t = 0; t < C::PPT; ++t) {
+        const int j = sj + t * C::TPR;
+        const float p = exp2f(sv[t] - m_new);
+        const uint16_t hi = f32_to_bf16_bits(p);
+        const uint16_t lo16 = f32_to_bf16_bits(p - bf16_bits_to_f32(hi));
+        phi[j] = hi;
+        plo[j] = lo16;
+        psum += p;
+      }
+#pragma unroll
+      for (int off = C::TPR / 2; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      if (sj == 0) sAlpha[sr] = alpha;
+    }
+    // rows [nv, nv16) of the V stage were not written by this tile's copies:
+    // zero them so 0-weight positions contribute exactly 0.
+    if (nv < nv16) {
+      const int words = (nv16 - nv) * (C::HS / 8);  // 16-byte words
+      for (int w16 = tid; w16 < words; w16 += C::CTHREADS) {
+        const int r = nv + w16 / (C::HS / 8), c = (w16 % (C::HS / 8)) * 8;
+        *reinterpret_cast<uint4*>(tV + r * C::PITCH + c) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();  // order before the next bulk copies into this stage
+    }
+    named_bar_sync(1, C::CTHREADS);
+
+    // ---- O^T[dim][row] = alpha * O^T + V^T P^T  (P split into bf16 hi + lo)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+      const float al0 = sAlpha[nt * 8 + 2 * t4], al1 = sAlpha[nt * 8 + 2 * t4 + 1];
+#pragma unroll
+      for (int mt = 0; mt < C::KD; ++mt) {
+        o[mt][nt][0] *= al0;
+        o[mt][nt][1] *= al1;
+        o[mt][nt][2] *= al0;
+        o[mt][nt][3] *= al1;
+      }
+    }
+#pragma unroll
+    for (int kp = 0; kp < C::MP; ++kp) {
+      if (kp * 16 < nv16) {
+        uint32_t pb[C::NT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+          // matrices: (hi, pos 0-7), (hi, pos 8-15), (lo, pos 0-7), (lo, pos 8-15); rows = query rows
+          const uint16_t* pa = sP + ((lmat >> 1) * C::NP + nt * 8 + lrow) * C::PPITCH + kp * 16 + (lmat & 1) * 8;
+          ldsm_x4(smem_u32(pa), pb[nt][0], pb[nt][1], pb[nt][2], pb[nt][3]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::KD; ++mt) {
+          // V^T fragments: matrices (d 0-7, pos 0-7), (d 8-15, pos 0-7), (d 0-7, pos 8-15), (d 8-15, pos 8-15)
+          const int prow = kp * 16 + lrow + (lmat >> 1) * 8;
+          const int dcol = dbase + mt * 16 + (lmat & 1) * 8;
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_trans(smem_u32(tV + prow * C::PITCH + dcol), v0, v1, v2, v3);
+#pragma unroll
+          for (int nt = 0; nt < C::NT; ++nt) {
+            mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+            mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][2], pb[nt][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+  }
+
+  // ---- epilogue: partial (O, m, l) or, with one split, the normalised row
+  if (sr < G && sj == 0) {
+    sM[sr] = m_run;
+    sL[sr] = l_run;
+  }
+  named_bar_sync(1, C::CTHREADS);
+#pragma unroll
+  for (int mt = 0; mt < C::KD; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = nt * 8 + 2 * t4 + (e & 1);
+        if (r >= G) continue;
+        const int d = dbase + mt * 16 + grp + (e >> 1) * 8;
+        const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
+        if (direct) {
+          const float val = o[mt][nt][e] / sL[r];
+          a.out[row * C::HS + d] = f32_to_bf16_bits(val);
+          if (a.out_f32) a.out_f32[row * C::HS + d] = val;
+        } else {
+          a.ws_o[(row * a.num_splits + s) * C::HS + d] = o[mt][nt][e];
+        }
+      }
+  if (!direct && tid < G) {
+    const size_t r = ((static_cast<size_t>(b) * a.NH + hbase + tid) * a.num_splits + s) * 2;
+    a.ws_ml[r] = sM[tid];
+    a.ws_ml[r + 1] = sL[tid];
+  }
+}
+
+// ================================================================ merge kernel
+
+constexpr int kMergeWarps = 8;
+
+// One block per (32-dim slab, query head, sequence). Lane = dim in the slab,
+// warp w = splits w, w + 8, ...; M = max_s m_s, w_s = 2^(m_s - M),
+// out = sum_s w_s O_s / sum_s w_s l_s.
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
+  __shared__ float sacc[kMergeWarps][32];
+  __shared__ float sl[kMergeWarps];
+  const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int lo;
+  const int band = band_of(a.lens[b], a.capacity, a.window, false, &lo);
+  const int chunk = chunk_of(band, a.num_splits, a.granule);
+  const int ns = active_splits(band, chunk);
+  const size_t row = static_cast<size_t>(b) * a.NH + h;
+  const float* ml = a.ws_ml + row * a.num_splits * 2;
+  const int d = slab * 32 + lane;
+
+  float M = kNegInf;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc = 0.f, lsum = 0.f;
+  const float* ob = a.ws_o + row * a.num_splits * a.HS + d;
+  for (int s = warp; s < ns; s += kMergeWarps) {
+    const float w = exp2f(ml[2 * s] - M);
+    lsum += w * ml[2 * s + 1];
+    acc += w * ob[static_cast<size_t>(s) * a.HS];
+  }
+  sacc[warp][lane] = acc;
+  if (lane == 0) sl[warp] = lsum;
+  __syncthreads();
+  if (warp == 0) {
+    float t = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) {
+      t += sacc[w][lane];
+      L += sl[w];
+    }
+    const float val = ns > 0 ? t / L : 0.f;
+    a.out[row * a.HS + d] = f32_to_bf16_bits(val);
+    if (a.out_f32) a.out_f32[row * a.HS + d] = val;
+  }
+}
+
+// ================================================================ dispatch
+
+template <class C>
+cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
+  static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_splits, a.NKV, a.B);
+  split_tc_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t occupancy_tc(int* ctas) {
+  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
+}
+
+// Tile configurations: about 32 KB of K+V per pipeline stage, three stages.
+using Tc64x1 = TcCfg<64, 1, 96, 4, 3>;
+using Tc64x2 = TcCfg<64, 2, 96, 4, 3>;
+using Tc128x1 = TcCfg<128, 1, 48, 4, 3>;
+using Tc128x2 = TcCfg<128, 2, 48, 4, 3>;
+using Tc256x1 = TcCfg<256, 1, 32, 4, 3>;
+using Tc256x2 = TcCfg<256, 2, 32, 4, 3>;
+using Tc512x1 = TcCfg<512, 1, 16, 4, 3>;
+using Tc512x2 = TcCfg<512, 2, 16, 4, 3>;
+
+template <template <class> class Fn, class... Args>
+cudaError_t with_tc_cfg(int HS, int G, Args&&... args) {
+  const bool two = G > 8;
+  switch (HS) {
+    case 64: return two ? Fn<Tc64x2>::run(args...) : Fn<Tc64x1>::run(args...);
+    case 128: return two ? Fn<Tc128x2>::run(args...) : Fn<Tc128x1>::run(args...);
+    case 256: return two ? Fn<Tc256x2>::run(args...) : Fn<Tc256x1>::run(args...);
+    case 512: return two ? Fn<Tc512x2>::run(args...) : Fn<Tc512x1>::run(args...);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class C>
+struct LaunchFn {
+  static cudaError_t run(const LaunchArgs& a, cudaStream_t s) { return launch_tc<C>(a, s); }
+};
+template <class C>
+struct OccFn {
+  static cudaError_t run(int* ctas) { return occupancy_tc<C>(ctas); }
+};
+
+}  // namespace
+
+int tc_tile_positions(int HS) {
+  switch (HS) {
+    case 64: return Tc64x1::T;
+    case 128: return Tc128x1::T;
+    case 256: return Tc256x1::T;
+    case 512: return Tc512x1::T;
+    default: return 16;
+  }
+}
+
+// Chunks need no rounding: rows are copied one by one, so a split may start at
+// any position, and a partial last tile is masked.
+int plan_granule(int path, int HS) {
+  (void)path;
+  (void)HS;
+  return 1;
+}
+
+cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas) {
+  if (path == FD_PATH_SIMT) {
+    const size_t sm = simt_smem_bytes(G, HS);
+    cudaError_t e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_simt_kernel, kSimtThreads, sm);
+  }
+  return with_tc_cfg<OccFn>(HS, G, ctas);
+}
+
+cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
+  const int G = a.NH / a.NKV;
+  cudaError_t e;
+  if (a.path == FD_PATH_SIMT) {
+    const size_t sm = simt_smem_bytes(G, a.HS);
+    e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.num_splits, a.NKV, a.B);
+    split_simt_kernel<<<grid, kSimtThreads, sm, stream>>>(a);
+    e = cudaGetLastError();
+  } else {
+    e = with_tc_cfg<LaunchFn>(a.HS, G, a, stream);
+  }
+  if (e != cudaSuccess || a.num_splits == 1) return e;
+  dim3 mgrid(a.HS / 32, a.NH, a.B);
+  merge_kernel<<<mgrid, kMergeWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  *err = v;
+  return e;
+}
+
+}  // namespace fd

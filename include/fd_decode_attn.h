@@ -1,0 +1,195 @@
+/*
+ * fd_decode_attn.h - C ABI of libfd.so: single-token split-KV decode attention
+ * (Flash-Decoding) over a position-addressed bf16 KV cache, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * What the library computes is defined in "Hand-Writing Gemma 4
+ * Flash-Decoding + an FP4 Matvec Bonus (Part 2)", section "One KV head breaks
+ * the textbook": one query token per sequence attends over its KV cache with
+ * GQA/MQA grouping; the kernel walks absolute positions, reading position pos
+ * from slot pos % capacity, and reads only the live band
+ * [max(0, len - window), len); the key sequence is split across thread blocks
+ * whose unnormalised (O, m, l) partials are combined by an online-softmax
+ * merge ("fixup") kernel. For every sequence b and query head h:
+ *
+ *     kvh   = h / (NH / NKV)
+ *     band  = [max(0, len_b - min(W, capacity)), len_b),  W = window or infinity
+ *     s_p   = scale * dot(q[b][h], K[b][kvh][p % capacity])   for p in band
+ *     out[b][h] = sum_p softmax(s)_p * V[b][kvh][p % capacity]
+ *
+ * len_b == 0 gives an all-zero output row.
+ *
+ * Conventions shared by every entry point:
+ *   - Return value: FD_OK (0) or one of the FD_ERR_* codes below. No C++
+ *     exception crosses this boundary. On any error nothing is launched.
+ *   - All tensors are caller-owned DEVICE memory of the current CUDA device,
+ *     row-major, densely packed:
+ *       q        bf16  [B][NH][HS]          (= [B, 1, NH*HS]; Q head h of
+ *                                            group kvh is row kvh*G + h%G)
+ *       k_cache  bf16  [B][NKV][capacity][HS]   position p of sequence b lives
+ *       v_cache  bf16  [B][NKV][capacity][HS]   in row (b, kvh, p % capacity)
+ *       out      bf16  [B][NH][HS]          rounded to nearest even
+ *       out_f32  fp32  [B][NH][HS]          optional copy before rounding
+ *       lens     int32 [B]                  len_b, counting the current token
+ *     q, k_cache, v_cache, out, out_f32 and the workspace must be 16-byte
+ *     aligned, lens 4-byte aligned (else FD_ERR_ALIGNMENT).
+ *   - Supported shapes: HS in {64, 128, 256, 512}; NH % NKV == 0 and
+ *     G = NH / NKV <= 16; capacity >= 1; window <= 0 means no window, and
+ *     window > capacity is rejected (FD_ERR_INVALID_ARG). B == 0 is a no-op.
+ *   - scale <= 0 selects 1/sqrt(HS) (the attnScale convention of
+ *     SharpInference issue #156, "Background").
+ *   - Launches are asynchronous on `stream`; no entry point that launches
+ *     work synchronises the host, so a call can be captured in a CUDA graph
+ *     once its workspace exists. `lens` is read on the device, so replays of
+ *     a captured call see the current lengths.
+ *   - Lengths that break the cache's precondition are repaired on the device
+ *     and reported through the device error word (fd_get_device_error):
+ *     len_b < 0 is treated as 0; with no window, len_b > capacity keeps the
+ *     last `capacity` positions.
+ */
+#ifndef FD_DECODE_ATTN_H_
+#define FD_DECODE_ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* fd_stream_t;
+
+enum {
+  FD_OK = 0,
+  FD_ERR_INVALID_ARG = 1,   /* null pointer, bad size, window > capacity, bad plan */
+  FD_ERR_UNSUPPORTED = 2,   /* HS not in {64,128,256,512}, NH % NKV != 0, G > 16 */
+  FD_ERR_ALIGNMENT = 3,     /* a pointer is not aligned as required */
+  FD_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+  FD_ERR_WORKSPACE = 5      /* workspace too small, or would need allocating during capture */
+};
+
+/* Bits of the device error word (fd_get_device_error). */
+enum {
+  FD_DEVERR_LEN_NEGATIVE = 1u << 0,  /* some len_b < 0; treated as 0 */
+  FD_DEVERR_LEN_CLAMPED = 1u << 1,   /* no window and len_b > capacity; band clamped */
+  FD_DEVERR_WAIT_TIMEOUT = 1u << 2   /* a pipeline wait gave up; the output is invalid */
+};
+
+/* Kernel families. */
+enum {
+  FD_PATH_AUTO = 0,   /* let the plan choose */
+  FD_PATH_SIMT = 1,   /* plain per-position fp32 kernel; reference GPU path */
+  FD_PATH_TC = 2      /* bulk-copy pipelined, tensor-core (mma) tile kernel */
+};
+
+/*
+ * Launch plan: how many key-sequence splits each (sequence, KV head) gets and
+ * how much workspace the split partials need. Built by fd_plan / fd_plan_sms;
+ * the caller may change num_splits and path through fd_plan_override only.
+ *
+ * Split rule (the page gives none; "One KV head breaks the textbook" only says
+ * to split the key sequence across blocks so one KV head still fills the GPU):
+ * units U = B * NKV; enough splits that U * num_splits covers every CTA slot of
+ * the GPU once; a split then never exceeds `max_chunk` positions (a bound that
+ * keeps ragged batches balanced), rounding num_splits up to a whole number of
+ * waves when that bound applies. On the device each sequence cuts its own band
+ * into chunks of ceil(band_b / num_splits) rounded up to `granule` positions,
+ * so a short sequence uses fewer, not emptier, splits.
+ */
+typedef struct {
+  int num_splits;          /* S: grid splits per (sequence, KV head) */
+  int path;                /* FD_PATH_SIMT or FD_PATH_TC */
+  int granule;             /* chunk rounding on the device, positions */
+  int max_band;            /* band bound the plan was sized for */
+  int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
+  int num_sms;             /* SM count the plan assumed */
+  size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
+  /* the shape the plan was made for; fd_decode_attn_ex checks it */
+  int B, NH, NKV, HS, capacity, window;
+} fd_plan_t;
+
+/*
+ * fd_plan: build a plan for the given shape on CUDA device `device` (its SM
+ * count and the kernel's occupancy are queried). max_len > 0 bounds len_b
+ * (tighter plans for short contexts); max_len <= 0 uses the largest band the
+ * cache can hold, min(window, capacity). Pure host computation plus device
+ * attribute queries; launches nothing and allocates nothing.
+ * Errors: FD_ERR_INVALID_ARG, FD_ERR_UNSUPPORTED, FD_ERR_CUDA (query failed).
+ */
+int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
+            int device, fd_plan_t* plan);
+
+/*
+ * fd_plan_sms: the same plan for a GPU with `num_sms` SMs and `ctas_per_sm`
+ * resident CTAs per SM, without touching any device (for tools and tests).
+ */
+int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
+                int num_sms, int ctas_per_sm, fd_plan_t* plan);
+
+/*
+ * fd_plan_override: force the split count (num_splits >= 1; 0 keeps the
+ * plan's) and/or the kernel family (path != FD_PATH_AUTO), recomputing
+ * workspace_bytes. Used to test that the result does not depend on the split
+ * count, and to bisect. Errors: FD_ERR_INVALID_ARG.
+ */
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path);
+
+/*
+ * fd_workspace_bytes: workspace the split partials of a plan need:
+ * B * NH * num_splits * (HS + 2) * 4 bytes, rounded up to 256 (0 when
+ * num_splits == 1, where the split kernel writes the output itself).
+ */
+size_t fd_workspace_bytes(const fd_plan_t* plan);
+
+/*
+ * fd_decode_attn: the whole hot path in one call - split kernel, then merge
+ * kernel - with a plan made for the current device (max_len <= 0) and a
+ * workspace the library owns, one per (device, stream), grown on demand and
+ * kept until fd_release. The first call for a (device, stream) and shape
+ * allocates with cudaMalloc (which synchronises the device) and must not be
+ * made while the stream is being captured; later calls with shapes needing no
+ * more workspace allocate nothing and may be captured. Capture with a
+ * too-small workspace returns FD_ERR_WORKSPACE.
+ * Errors: every FD_ERR_* code.
+ */
+int fd_decode_attn(const void* q, const void* k_cache, const void* v_cache, void* out,
+                   const int* lens, int B, int NH, int NKV, int HS, int capacity,
+                   int window, float scale, fd_stream_t stream);
+
+/*
+ * fd_decode_attn_ex: the same with an explicit plan, a caller-owned device
+ * workspace of workspace_bytes >= fd_workspace_bytes(plan) (contents need no
+ * initialisation and are scratch between calls; calls that overlap on the GPU
+ * must not share one), and an optional fp32 copy of the output (out_f32 may be
+ * NULL). The shape arguments must equal the plan's. Allocates nothing.
+ * Errors: every FD_ERR_* code.
+ */
+int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes,
+                      float* out_f32, const void* q, const void* k_cache,
+                      const void* v_cache, void* out, const int* lens, int B, int NH,
+                      int NKV, int HS, int capacity, int window, float scale,
+                      fd_stream_t stream);
+
+/*
+ * fd_get_device_error: wait for `stream`, then return in *err the OR of the
+ * FD_DEVERR_* bits raised on the current device since the last read, and
+ * clear them. Synchronises the host: for tests and diagnostics only.
+ * Errors: FD_ERR_INVALID_ARG (err NULL), FD_ERR_CUDA.
+ */
+int fd_get_device_error(fd_stream_t stream, unsigned int* err);
+
+/* fd_release: free the library-owned workspaces of every device. Not
+ * thread-safe against concurrent fd_decode_attn calls. */
+void fd_release(void);
+
+/* fd_strerror: static, human-readable text for an FD_* status code. */
+const char* fd_strerror(int status);
+
+/* fd_version: (major << 16) | (minor << 8) | patch. */
+int fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_DECODE_ATTN_H_ */

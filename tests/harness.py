@@ -1,0 +1,106 @@
+"""GPU test harness: runs libfd.so through the C ABI with guarded buffers and
+compares with the FP64 oracle.
+
+Tolerances (the stated acceptance bar for this op):
+  * fp32 output (before the bf16 store) vs oracle: max |err| <= 2e-3;
+  * bf16 output vs the oracle rounded to bf16: |err| <= 1 bf16 ulp + 1e-3.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import decode_attention_04_gb300 as fd
+import oracle
+
+ATOL_F32 = 2e-3
+BF16_EXTRA = 1e-3
+GUARD = 4096          # bytes of canary on each side of every output buffer
+CANARY = 0xA5
+
+
+class Guarded:
+    """A device buffer with canary bytes before and after the usable region."""
+
+    def __init__(self, nbytes: int, device, fill: int | None = None):
+        self.nbytes = nbytes
+        self.raw = torch.full((GUARD + max(nbytes, 1) + GUARD,), CANARY, dtype=torch.uint8, device=device)
+        self.body = self.raw[GUARD:GUARD + max(nbytes, 1)]
+        if fill is not None:
+            self.body.fill_(fill)
+
+    def view(self, dtype, shape):
+        return self.body[: self.nbytes].view(dtype).view(shape)
+
+    def ptr(self) -> int:
+        return self.body.data_ptr()
+
+    def canaries_intact(self) -> bool:
+        lo = self.raw[:GUARD]
+        hi = self.raw[GUARD + max(self.nbytes, 1):]
+        return bool((lo == CANARY).all().item() and (hi == CANARY).all().item())
+
+
+def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len: int = 0,
+        poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None):
+    """One fd_decode_attn_ex call. Returns dict with out (bf16, cpu), out32
+    (fp32, cpu), plan, deverr, canaries (bool)."""
+    dev = torch.device(device)
+    if inputs_on_device:
+        qd, kd, vd, ld = q, k, v, lens.to(dev)
+    else:
+        qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len)
+    if splits or path:
+        fd.fd_plan_override(plan, splits, path)
+    n = w.B * w.NH * w.HS
+    o16 = Guarded(n * 2, dev, fill=0xFF)         # NaN-filled: unwritten rows show up
+    o32 = Guarded(n * 4, dev, fill=0xFF)
+    ws = Guarded(plan.workspace_bytes, dev, fill=0xFF if poison_ws else 0)
+    fd.fd_get_device_error()  # clear
+    fd.fd_decode_attn_ex(plan, ws.ptr() if plan.workspace_bytes else None, plan.workspace_bytes, o32.ptr(),
+                         qd, kd, vd, o16.ptr(), ld, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
+                         w.scale if scale is None else scale)
+    torch.cuda.synchronize()
+    err = fd.fd_get_device_error()
+    return dict(out=o16.view(torch.bfloat16, (w.B, w.NH, w.HS)).cpu(),
+                out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(),
+                plan=plan, deverr=err,
+                canaries=o16.canaries_intact() and o32.canaries_intact() and ws.canaries_intact())
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits); subnormal floor 2^-133."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.exp2(np.maximum(e, -126) - 7), 2.0 ** -133)
+
+
+def check(res: dict, ref: np.ndarray, rows=None, what: str = ""):
+    """Assert the GPU result matches the oracle within the tolerances, on all
+    rows or on the (b, h) pairs in `rows`."""
+    assert res["canaries"], f"{what}: guard canary overwritten"
+    out32 = res["out32"].double().numpy()
+    out16 = res["out"].view(torch.int16).numpy().view(np.uint16)
+    if rows is not None:
+        idx = tuple(np.array(rows).T)
+        out32, out16, ref = out32[idx], out16[idx], ref[idx]
+    assert np.isfinite(out32).all(), f"{what}: non-finite fp32 output"
+    e32 = np.abs(out32 - ref).max()
+    assert e32 <= ATOL_F32, f"{what}: fp32 max abs err {e32:.3e} > {ATOL_F32}"
+    ref16 = oracle.bf16_bits_to_f64(oracle.bf16_round(ref))
+    got16 = oracle.bf16_bits_to_f64(out16)
+    lim = bf16_ulp(ref16) + BF16_EXTRA
+    bad = np.abs(got16 - ref16) > lim
+    assert not bad.any(), f"{what}: {bad.sum()} bf16 outputs beyond 1 ulp + 1e-3 (max {np.abs(got16 - ref16).max():.3e})"
+    return e32
+
+
+def oracle_ref(w, q, k, v, lens, rows=None):
+    want = None
+    if rows is not None:
+        want = np.zeros(w.B * w.NH, dtype=bool)
+        for b, h in rows:
+            want[b * w.NH + h] = True
+    return oracle.decode(q, k, v, lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale, want=want)

@@ -1,0 +1,161 @@
+"""C-ABI checks that need no GPU: libfd.so loads, exports every entry point
+include/fd_decode_attn.h declares, plans as documented, and rejects bad
+arguments before making any CUDA call."""
+
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import decode_attention_04_gb300 as fd
+from decode_attention_04_gb300.inputs import WORKLOADS
+
+ROOT = Path(__file__).resolve().parent.parent
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_attention_04_gb300 import build
+    build.build()
+    return fd.load_library()
+
+
+def _declared():
+    names = set()
+    for h in (ROOT / "include").glob("*.h"):
+        text = re.sub(r"/\*.*?\*/", "", h.read_text(), flags=re.S)
+        names |= set(re.findall(r"\b(fd_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_boundary():
+    d = _declared()
+    for n in ("fd_plan", "fd_decode_attn", "fd_decode_attn_ex", "fd_strerror", "fd_get_device_error"):
+        assert n in d
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding wraps every one of them under the same name
+    for n in _declared():
+        assert callable(getattr(fd, n)), n
+
+
+def test_strerror_and_version(lib):
+    assert fd.fd_strerror(fd.FD_OK) == "ok"
+    for c in (1, 2, 3, 4, 5):
+        assert fd.fd_strerror(c) and fd.fd_strerror(c) != "unknown status"
+    assert fd.fd_strerror(99) == "unknown status"
+    assert fd.fd_version() > 0
+
+
+def _plan(w, sms=152, ctas=2, max_len=0):
+    return fd.fd_plan_sms(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len, sms, ctas)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_plan_fills_the_gpu_and_sizes_workspace(name, lib):
+    w = WORKLOADS[name]
+    p = _plan(w)
+    units = w.B * w.NKV
+    band = min(w.window if w.window > 0 else w.capacity, w.capacity)
+    assert p.max_band == band
+    # every CTA slot of the GPU gets work at the bound the plan was sized for
+    chunk = -(-band // p.num_splits)
+    chunk = -(-chunk // p.granule) * p.granule
+    active = -(-band // chunk)
+    # (granule rounding may leave a few percent of the slots idle)
+    assert units * active >= 0.9 * min(152 * 2, units * -(-band // p.granule))
+    expect_ws = 0 if p.num_splits == 1 else (
+        -(-(w.B * w.NH * p.num_splits * w.HS * 4) // 256) * 256 + -(-(w.B * w.NH * p.num_splits * 8) // 256) * 256)
+    assert p.workspace_bytes == expect_ws == fd.fd_workspace_bytes(p)
+    # workspace is bounded by partials, never by the cache allocation
+    assert p.workspace_bytes <= 32 << 20
+
+
+def test_plan_mqa_one_kv_head_uses_every_sm(lib):
+    w = WORKLOADS["gemma_global_mqa_32k"]
+    p = _plan(w)
+    assert p.num_splits >= 152  # one KV head still spreads over all SMs
+
+
+def test_plan_max_len_tightens_short_context(lib):
+    w = WORKLOADS["gemma_global_mqa_4k"]
+    full = _plan(w)
+    short = _plan(w, max_len=4096)
+    assert short.max_band == 4096 < full.max_band
+    assert short.workspace_bytes <= full.workspace_bytes
+
+
+def test_plan_balance_bound_for_ragged_batches(lib):
+    w = WORKLOADS["llama_ragged"]
+    p = _plan(w)
+    chunk = -(-w.capacity // p.num_splits)
+    assert chunk * w.HS * 4 <= (2 << 20) + p.granule * w.HS * 4
+    assert p.num_splits % max(1, -(-(152 * 2) // (w.B * w.NKV))) == 0  # whole waves
+
+
+def test_plan_override(lib):
+    w = WORKLOADS["gemma_local_ring"]
+    p = _plan(w)
+    fd.fd_plan_override(p, 1, fd.FD_PATH_SIMT)
+    assert p.num_splits == 1 and p.path == fd.FD_PATH_SIMT and p.workspace_bytes == 0
+    fd.fd_plan_override(p, 7, fd.FD_PATH_TC)
+    assert p.num_splits == 7 and p.path == fd.FD_PATH_TC and p.workspace_bytes > 0
+    with pytest.raises(fd.FdError):
+        fd.fd_plan_override(p, -1, 0)
+    with pytest.raises(fd.FdError):
+        fd.fd_plan_override(p, 0, 9)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 16, 8, 96, 64, 0), fd.FD_ERR_UNSUPPORTED),     # HS
+    ((1, 12, 8, 128, 64, 0), fd.FD_ERR_UNSUPPORTED),    # NH % NKV
+    ((1, 64, 2, 128, 64, 0), fd.FD_ERR_UNSUPPORTED),    # G = 32 > 16
+    ((1, 16, 8, 128, 64, 65), fd.FD_ERR_INVALID_ARG),   # window > capacity
+    ((1, 16, 8, 128, 0, 0), fd.FD_ERR_INVALID_ARG),     # capacity
+    ((-1, 16, 8, 128, 64, 0), fd.FD_ERR_INVALID_ARG),   # B
+    ((1, 0, 8, 128, 64, 0), fd.FD_ERR_INVALID_ARG),     # NH
+])
+def test_shape_errors_before_any_cuda_call(lib, args, code):
+    B, NH, NKV, HS, cap, win = args
+    p = fd.fd_plan_t()
+    assert lib.fd_plan_sms(B, NH, NKV, HS, cap, win, 0, 152, 2, ctypes.byref(p)) == code
+    # fd_decode_attn checks the shape before it touches the device
+    assert lib.fd_decode_attn(16, 16, 16, 16, 16, B, NH, NKV, HS, cap, win, 0.0, None) == code
+
+
+def test_pointer_and_workspace_errors_before_any_cuda_call(lib):
+    w = WORKLOADS["gemma_local_ring"]
+    p = _plan(w)
+    args = (w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
+    A = 1 << 20  # fake, aligned addresses; nothing is dereferenced on these paths
+    ex = lib.fd_decode_attn_ex
+    # null tensor
+    assert ex(ctypes.byref(p), A, p.workspace_bytes, None, None, A, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    # misaligned q / lens / out_f32
+    assert ex(ctypes.byref(p), A, p.workspace_bytes, None, A + 2, A, A, A, A, *args) == fd.FD_ERR_ALIGNMENT
+    assert ex(ctypes.byref(p), A, p.workspace_bytes, None, A, A, A, A, A + 2, *args) == fd.FD_ERR_ALIGNMENT
+    assert ex(ctypes.byref(p), A, p.workspace_bytes, A + 4, A, A, A, A, A, *args) == fd.FD_ERR_ALIGNMENT
+    # workspace missing / too small / misaligned
+    assert ex(ctypes.byref(p), None, 0, None, A, A, A, A, A, *args) == fd.FD_ERR_WORKSPACE
+    assert ex(ctypes.byref(p), A, p.workspace_bytes - 1, None, A, A, A, A, A, *args) == fd.FD_ERR_WORKSPACE
+    assert ex(ctypes.byref(p), A + 8, p.workspace_bytes, None, A, A, A, A, A, *args) == fd.FD_ERR_ALIGNMENT
+    # shape that disagrees with the plan
+    bad = (w.B, w.NH, w.NKV, w.HS, w.capacity * 2, w.window, 0.0, None)
+    assert ex(ctypes.byref(p), A, p.workspace_bytes, None, A, A, A, A, A, *bad) == fd.FD_ERR_INVALID_ARG
+    # null plan
+    assert ex(None, A, p.workspace_bytes, None, A, A, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    # B == 0 is a no-op success
+    p0 = fd.fd_plan_sms(0, 16, 8, 256, 64, 0, 0, 152, 2)
+    assert ex(ctypes.byref(p0), None, 0, None, None, None, None, None, None,
+              0, 16, 8, 256, 64, 0, 0.0, None) == fd.FD_OK
+    assert lib.fd_get_device_error(None, None) == fd.FD_ERR_INVALID_ARG
+
+
+def test_binding_raises_fderror(lib):
+    with pytest.raises(fd.FdError) as e:
+        fd.fd_plan_sms(1, 16, 8, 96, 64, 0, 0, 152, 2)
+    assert e.value.status == fd.FD_ERR_UNSUPPORTED

@@ -1,0 +1,231 @@
+"""GPU parity of libfd.so against the FP64 oracle, through the C ABI.
+
+Fixture categories follow "Hand-Writing Gemma 4 Flash-Decoding + an FP4 Matvec
+Bonus (Part 2)", section "The test that catches what parity misses": split
+boundaries, pre-window positions, ring wrap, batch > 1; every cache slot
+outside the live band holds NaN, every output buffer is guarded by canaries,
+and the workspace starts filled with NaN bytes so an unwritten partial would
+surface.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_04_gb300 as fd
+from decode_attention_04_gb300.inputs import WORKLOADS, Workload, make_inputs
+from harness import check, oracle_ref, run
+
+pytestmark = pytest.mark.gpu
+
+W = Workload
+
+FIXTURES = [
+    # ---- split boundaries (band vs tile / chunk edges)
+    W("band1_mqa", 1, 16, 1, 512, 64, 0, lens=(1,), seed=1),
+    W("band2_ring", 1, 16, 8, 256, 64, 0, lens=(2,), seed=2),
+    W("tile_minus1_d256", 1, 16, 8, 256, 64, 0, lens=(31,), seed=3),
+    W("tile_exact_d256", 1, 16, 8, 256, 64, 0, lens=(32,), seed=4),
+    W("tile_plus1_d256", 1, 16, 8, 256, 64, 0, lens=(33,), seed=5),
+    W("tile_pm1_d512", 2, 16, 1, 512, 64, 0, lens=(15, 17), seed=6),
+    W("tile_pm1_d128", 2, 32, 8, 128, 128, 0, lens=(47, 49), seed=7),
+    W("tile_pm1_d64", 2, 8, 8, 64, 256, 0, lens=(95, 97), seed=8),
+    # ---- pre-window positions
+    W("len_below_window", 1, 16, 8, 256, 64, 48, lens=(40,), seed=9),
+    W("len_equal_window", 1, 16, 8, 256, 64, 48, lens=(48,), seed=10),
+    W("len_window_plus1", 1, 16, 8, 256, 64, 48, lens=(49,), seed=11),
+    W("lo_not_tile_aligned", 1, 16, 1, 512, 128, 37, lens=(100,), seed=12),
+    # ---- ring wrap
+    W("ring_full_1024", 1, 16, 8, 256, 1024, 1024, lens=(1024,), seed=13),
+    W("ring_wrap_1025", 1, 16, 8, 256, 1024, 1024, lens=(1025,), seed=14),
+    W("ring_wrap_32x", 1, 16, 8, 256, 1024, 1024, lens=(32768,), seed=15),
+    W("ring_wrap_33000", 1, 16, 8, 256, 1024, 1024, lens=(33000,), seed=16),
+    W("ring_dead_slots_w1000", 1, 16, 8, 256, 1024, 1000, lens=(5000,), seed=17),
+    W("ring_straddles_slot0", 1, 16, 8, 256, 64, 64, lens=(100,), seed=18),
+    # ---- batch > 1
+    W("batch16_ragged_llama", 16, 32, 8, 128, 512, 0,
+      lens=(1, 512, 17, 300, 2, 511, 64, 65, 128, 129, 250, 3, 400, 33, 90, 256), seed=19),
+    W("batch4_mqa_with_empty", 4, 16, 1, 512, 512, 0, lens=(0, 1, 17, 300), seed=20),
+    W("batch3_ring_mixed", 3, 16, 8, 256, 128, 100, lens=(0, 99, 1000), seed=21),
+    # ---- other groupings and head sizes
+    W("mha_d64", 2, 8, 8, 64, 200, 0, lens=(200, 77), seed=22),
+    W("g8_d128", 1, 16, 2, 128, 300, 0, lens=(300,), seed=23),
+    W("g16_d64", 1, 16, 1, 64, 300, 0, lens=(299,), seed=24),
+    W("g4_d512", 1, 8, 2, 512, 200, 0, lens=(150,), seed=25),
+    W("g2_d128_window1", 2, 16, 8, 128, 64, 1, lens=(37, 1), seed=26),
+]
+
+
+@pytest.mark.parametrize("path", [fd.FD_PATH_TC, fd.FD_PATH_SIMT], ids=["tc", "simt"])
+@pytest.mark.parametrize("w", FIXTURES, ids=[f.name for f in FIXTURES])
+def test_fixture_matches_oracle(w, path):
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    res = run(w, q, k, v, lens, path=path)
+    check(res, ref, what=w.name)
+    assert res["deverr"] == 0
+
+
+SPLIT_CASES = [
+    W("split_mqa", 2, 16, 1, 512, 700, 0, lens=(700, 333), seed=31),
+    W("split_ring", 1, 16, 8, 256, 256, 200, lens=(1234,), seed=32),
+    W("split_llama", 3, 32, 8, 128, 400, 0, lens=(400, 1, 123), seed=33),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT_CASES, ids=[c.name for c in SPLIT_CASES])
+def test_result_independent_of_split_count(w):
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    band = max(min(int(x), w.window if w.window > 0 else w.capacity) for x in lens)
+    outs = []
+    for s in sorted({1, 2, 3, 7, 64, band, band + 5}):
+        res = run(w, q, k, v, lens, splits=s)
+        check(res, ref, what=f"{w.name} S={s}")
+        outs.append(res["out32"])
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2e-3
+
+
+def test_single_position_band_returns_v_exactly():
+    for w, slot in [(W("len1", 1, 16, 8, 256, 64, 0, lens=(1,), seed=41), 0),
+                    (W("win1", 1, 16, 1, 512, 64, 1, lens=(150,), seed=42), 149 % 64)]:
+        q, k, v, lens = make_inputs(w)
+        for path in (fd.FD_PATH_TC, fd.FD_PATH_SIMT):
+            for splits in (0, 1, 5):
+                res = run(w, q, k, v, lens, splits=splits, path=path)
+                G = w.NH // w.NKV
+                for h in range(w.NH):
+                    vrow = v[0, h // G, slot]
+                    assert torch.equal(res["out32"][0, h], vrow.float()), (w.name, path, splits, h)
+                    assert torch.equal(res["out"][0, h].view(torch.int16), vrow.view(torch.int16))
+
+
+def test_nan_inside_band_reaches_only_its_group():
+    w = W("nan_in_band", 1, 16, 8, 256, 256, 0, lens=(200,), seed=43)
+    q, k, v, lens = make_inputs(w)
+    k = k.clone()
+    k[0, 3, 77, 10] = float("nan")
+    res = run(w, q, k, v, lens)
+    o = res["out32"][0]
+    G = 2
+    assert torch.isnan(o[3 * G:4 * G]).all()
+    rest = torch.cat([o[:3 * G], o[4 * G:]])
+    assert torch.isfinite(rest).all()
+
+
+def test_repeat_runs_are_bitwise_identical():
+    w = W("determinism", 2, 16, 1, 512, 2048, 0, lens=(2048, 1111), seed=44)
+    q, k, v, lens = make_inputs(w)
+    dev = torch.device("cuda")
+    qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    first = None
+    for _ in range(100):
+        out = torch.empty_like(qd)
+        fd.fd_decode_attn_ex(plan, ws, plan.workspace_bytes, None, qd, kd, vd, out, ld, w.B, w.NH, w.NKV,
+                             w.HS, w.capacity, w.window, w.scale)
+        if first is None:
+            first = out.clone()
+        else:
+            assert torch.equal(out.view(torch.int16), first.view(torch.int16))
+
+
+def test_library_workspace_entry_equals_explicit_and_graph_replay():
+    """fd_decode_attn (library-owned workspace) == fd_decode_attn_ex, and a CUDA
+    graph replay of the call == the direct launch, bit for bit (the graph-parity
+    contract of SharpInference issue #156, Work Item B)."""
+    w = W("graph", 1, 16, 8, 256, 1024, 1024, lens=(5000,), seed=45)
+    q, k, v, lens = make_inputs(w)
+    dev = torch.device("cuda")
+    qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
+    res = run(w, q, k, v, lens)
+    s = torch.cuda.Stream()
+    out = torch.empty_like(qd)
+    with torch.cuda.stream(s):
+        fd.fd_decode_attn(qd, kd, vd, out, ld, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)  # warm-up
+    s.synchronize()
+    assert torch.equal(out.cpu().view(torch.int16), res["out"].view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    out_g = torch.zeros_like(qd)
+    with torch.cuda.graph(g, stream=s):
+        fd.fd_decode_attn(qd, kd, vd, out_g, ld, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g.view(torch.int16), out.view(torch.int16))
+    # lens live on the device: a replay sees new lengths
+    ld.fill_(3000)
+    g.replay()
+    torch.cuda.synchronize()
+    lens2 = torch.tensor([3000], dtype=torch.int32)
+    ref2 = oracle_ref(w, q, k, v, lens2)
+    assert np.abs(out_g.cpu().double().numpy() - ref2).max() <= 2e-2  # bf16 output
+
+
+def test_device_error_word_reports_repaired_lengths():
+    w = W("deverr", 2, 16, 8, 256, 64, 0, lens=(10, 10), seed=46)
+    q, k, v, _ = make_inputs(w, poison=False)
+    # negative length -> treated as 0 (zero output), flagged
+    res = run(w, q, k, v, torch.tensor([-5, 10], dtype=torch.int32))
+    assert res["deverr"] & fd.FD_DEVERR_LEN_NEGATIVE
+    assert torch.equal(res["out32"][0], torch.zeros_like(res["out32"][0]))
+    # no window, len > capacity -> the last `capacity` positions, flagged
+    lens = torch.tensor([150, 64], dtype=torch.int32)
+    res = run(w, q, k, v, lens)
+    assert res["deverr"] & fd.FD_DEVERR_LEN_CLAMPED
+    w2 = W("deverr_w", 2, 16, 8, 256, 64, 64, lens=(150, 64), seed=46)
+    res2 = run(w2, q, k, v, lens)
+    assert res2["deverr"] == 0
+    assert torch.equal(res["out32"], res2["out32"])
+
+
+def test_bad_arguments_launch_nothing():
+    w = WORKLOADS["llama_tiny"]
+    q, k, v, lens = make_inputs(w)
+    dev = torch.device("cuda")
+    qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
+    out = torch.full_like(qd, 7.0)
+    with pytest.raises(fd.FdError) as e:
+        fd.fd_decode_attn(qd, kd, vd, out, ld, w.B, w.NH, w.NKV, 96, w.capacity, w.window, w.scale)
+    assert e.value.status == fd.FD_ERR_UNSUPPORTED
+    raw = torch.empty(qd.numel() * 2 + 2, dtype=torch.uint8, device=dev)
+    with pytest.raises(fd.FdError) as e:
+        fd.fd_decode_attn(raw.data_ptr() + 2, kd, vd, out, ld, w.B, w.NH, w.NKV, w.HS, w.capacity,
+                          w.window, w.scale)
+    assert e.value.status == fd.FD_ERR_ALIGNMENT
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()
+
+
+# --------------------------------------------------- full-size workloads
+
+def _sample_rows(w, lens, n=8, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0), (w.B - 1, w.NH - 1)}
+    if w.B > 1:
+        L = lens.numpy()
+        rows |= {(int(L.argmin()), 0), (int(L.argmax()), w.NH // 2)}
+    while len(rows) < min(n, w.B * w.NH):
+        rows.add((int(rng.integers(w.B)), int(rng.integers(w.NH))))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_full_size_workload_sampled_rows(name):
+    """Full sizes in the launch configuration the benchmark times (fd_plan for
+    the device, max_len <= 0), inputs drawn on the device; the oracle checks a
+    sample of (sequence, head) rows, and every row is checked for finiteness
+    (the NaN poison outside the band)."""
+    w = WORKLOADS[name]
+    dev = torch.device("cuda")
+    q, k, v, lens = make_inputs(w, device=dev)
+    res = run(w, q, k, v, lens, inputs_on_device=True)
+    assert torch.isfinite(res["out32"]).all(), "NaN/inf in some row"
+    assert res["deverr"] == 0
+    rows = _sample_rows(w, lens)
+    qh, kh, vh = q.cpu(), k.cpu(), v.cpu()
+    del q, k, v
+    torch.cuda.empty_cache()
+    ref = oracle_ref(w, qh, kh, vh, lens, rows=rows)
+    check(res, ref, rows=rows, what=name)
