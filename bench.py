@@ -268,6 +268,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-geometries", action="store_true", help="skip the per-geometry table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="profiling mode: N plain fd_decode_attn calls on one layer of --workload, then exit")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -279,6 +281,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
+    if args.profile_calls:
+        return profile_calls(w, args.profile_calls)
 
     import decode_attention_04_gb300 as fd
     from decode_attention_04_gb300 import build as libbuild
@@ -396,6 +400,19 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def profile_calls(w, n):
+    """N plain calls on one layer (for ncu launch lists and captures)."""
+    from decode_attention_04_gb300 import build as libbuild
+    libbuild.build()
+    device = torch.device("cuda", 0)
+    st = Step(w, 1, device)
+    for _ in range(n):
+        st.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_calls": n, "workload": w.name, "live_bytes": st.live}), flush=True)
     return 0
 
 

@@ -23,6 +23,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <utility>
 
 #include "fd_decode_attn.h"
 #include "fd_internal.h"
@@ -145,6 +146,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start while the
+// previous kernel on the stream is still running. It must wait for that
+// kernel (and its memory) before reading any input; it lets the next kernel
+// launch once every one of its own blocks has started. Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -199,6 +214,8 @@ __global__ void __launch_bounds__(kSimtThreads) split_simt_kernel(const LaunchAr
   float* salpha = sl_run + G;        // [G]
   float* sp = salpha + G;            // [G]
 
+  grid_dependency_wait();
+  grid_launch_dependents();
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
@@ -325,6 +342,35 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hbase = kvh * G;
 
+  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + C::OFF_K);
+  uint16_t* sV = reinterpret_cast<uint16_t*>(smem + C::OFF_V);
+  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
+  uint16_t* sP = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
+  float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
+  float* sM = sAlpha + C::NP;
+  float* sL = sM + C::NP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::NSTAGE);
+
+  // Set-up that reads no input, overlapping the previous kernel's tail.
+  if (tid == 0) {
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(full0 + 8 * i, 32);         // every producer lane arrives once per phase
+      mbar_init(empty0 + 8 * i, C::NWC);    // one arrival per consumer warp
+    }
+    fence_mbar_init();
+  }
+  // Start P at zero and alpha at 1 so nothing read before its first write can
+  // carry a NaN bit pattern from uninitialised shared memory.
+  for (int i = tid; i < 2 * C::NP * C::PPITCH; i += C::THREADS) sP[i] = 0;
+  for (int i = tid; i < C::NP; i += C::THREADS) {
+    sAlpha[i] = 1.f;
+    sM[i] = kNegInf;
+    sL[i] = 0.f;
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
@@ -344,32 +390,6 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   const int n = static_cast<int>(p1 - p0);
   const int ntiles = (n + C::T - 1) / C::T;
-
-  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + C::OFF_K);
-  uint16_t* sV = reinterpret_cast<uint16_t*>(smem + C::OFF_V);
-  float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
-  uint16_t* sP = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
-  float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
-  float* sM = sAlpha + C::NP;
-  float* sL = sM + C::NP;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + C::NSTAGE);
-
-  if (tid == 0) {
-    for (int i = 0; i < C::NSTAGE; ++i) {
-      mbar_init(full0 + 8 * i, 32);         // every producer lane arrives once per phase
-      mbar_init(empty0 + 8 * i, C::NWC);    // one arrival per consumer warp
-    }
-    fence_mbar_init();
-  }
-  // P rows beyond G are never written by the softmax; keep them zero. alpha of
-  // those rows stays 1 so their (discarded) accumulators stay finite.
-  for (int i = tid; i < 2 * C::NP * C::PPITCH; i += C::THREADS) sP[i] = 0;
-  for (int i = tid; i < C::NP; i += C::THREADS) {
-    sAlpha[i] = 1.f;
-    sM[i] = kNegInf;
-    sL[i] = 0.f;
-  }
   __syncthreads();
 
   if (warp == C::NWC) {
@@ -473,8 +493,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
     named_bar_sync(1, C::CTHREADS);
 
-    // ---- one online-softmax update per row for the whole tile
-    if (sr < G) {
+    // ---- one online-softmax update per row for the whole tile. Every
+    // consumer thread takes part, padded rows (>= G, zero queries) included,
+    // so the full-warp shuffles below never run in a partial warp; padded rows
+    // only feed accumulator columns that are never stored.
+    {
       float sv[C::PPT];
       float tmax = kNegInf;
 #pragma unroll
@@ -613,6 +636,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   __shared__ float sl[kMergeWarps];
   const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dependency_wait();
+  grid_launch_dependents();
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, false, &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
@@ -651,6 +676,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
 
 // ================================================================ dispatch
 
+// Launch with programmatic stream serialization allowed, so this kernel's
+// blocks may be scheduled while the previous kernel on the stream drains; the
+// kernels above wait (griddepcontrol.wait) before touching any input.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <class C>
 cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
   static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
@@ -658,8 +702,7 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_splits, a.NKV, a.B);
-  split_tc_kernel<C><<<grid, C::THREADS, C::SMEM, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(split_tc_kernel<C>, grid, dim3(C::THREADS), C::SMEM, stream, a);
 }
 
 template <class C>
@@ -740,15 +783,13 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     dim3 grid(a.num_splits, a.NKV, a.B);
-    split_simt_kernel<<<grid, kSimtThreads, sm, stream>>>(a);
-    e = cudaGetLastError();
+    e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, a);
   } else {
     e = with_tc_cfg<LaunchFn>(a.HS, G, a, stream);
   }
   if (e != cudaSuccess || a.num_splits == 1) return e;
   dim3 mgrid(a.HS / 32, a.NH, a.B);
-  merge_kernel<<<mgrid, kMergeWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, a);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err) {
