@@ -22,6 +22,8 @@ FD_ERR_UNSUPPORTED = 2
 FD_ERR_ALIGNMENT = 3
 FD_ERR_CUDA = 4
 FD_ERR_WORKSPACE = 5
+FD_ERR_SCRATCH_LIMIT = 6
+FD_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 FD_DEVERR_LEN_NEGATIVE = 1 << 0
 FD_DEVERR_LEN_CLAMPED = 1 << 1
@@ -32,7 +34,8 @@ FD_PATH_SIMT = 1
 FD_PATH_TC = 2
 
 EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_override", "fd_workspace_bytes", "fd_decode_attn",
-            "fd_decode_attn_ex", "fd_get_device_error", "fd_release", "fd_strerror", "fd_version"]
+            "fd_decode_attn_ex", "fd_decode_attn_noalloc", "fd_get_device_error", "fd_release", "fd_strerror",
+            "fd_version"]
 
 
 class fd_plan_t(ctypes.Structure):
@@ -85,6 +88,7 @@ def load_library(path: Path | str | None = None):
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
                                    ctypes.c_float, vp]),
+        "fd_decode_attn_noalloc": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_get_device_error": (ci, [vp, ctypes.POINTER(ctypes.c_uint)]),
         "fd_release": (None, []),
         "fd_strerror": (ctypes.c_char_p, [ci]),
@@ -168,6 +172,17 @@ def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k
                                             _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
                                             _stream(stream)),
            "fd_decode_attn_ex")
+
+
+def fd_decode_attn_noalloc(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale,
+                           stream=None) -> None:
+    """fd_decode_attn for callers that must not allocate device memory while
+    they run: the split partials go to a fixed 32 MiB array inside libfd.so.
+    Calls that overlap on the GPU share that array and race; serialise them."""
+    _check(load_library().fd_decode_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lens),
+                                                 B, NH, NKV, HS, capacity, window, float(scale),
+                                                 _stream(stream)),
+           "fd_decode_attn_noalloc")
 
 
 def fd_get_device_error(stream=None) -> int:

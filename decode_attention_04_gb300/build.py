@@ -22,7 +22,7 @@ BUILD_DIR = PKG / "_build"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", str(INCLUDE), "-I", str(CSRC)] + ARCH
-SOURCES = ["fd_kernels.cu", "fd_api.cpp"]
+SOURCES = ["fd_kernels.cu", "fd_api.cpp", "fd_noalloc.cu"]
 
 
 def nvcc() -> str:

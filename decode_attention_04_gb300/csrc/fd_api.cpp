@@ -304,6 +304,8 @@ const char* fd_strerror(int status) {
     case FD_ERR_ALIGNMENT: return "pointer not aligned (16 bytes for tensors and workspace, 4 for lens)";
     case FD_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case FD_ERR_WORKSPACE: return "workspace too small, or would need allocating while the stream is captured";
+    case FD_ERR_SCRATCH_LIMIT:
+      return "shape needs more split-partial scratch than the fixed 32 MiB array of fd_decode_attn_noalloc";
     default: return "unknown status";
   }
 }

@@ -65,8 +65,12 @@ enum {
   FD_ERR_UNSUPPORTED = 2,   /* HS not in {64,128,256,512}, NH % NKV != 0, G > 16 */
   FD_ERR_ALIGNMENT = 3,     /* a pointer is not aligned as required */
   FD_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
-  FD_ERR_WORKSPACE = 5      /* workspace too small, or would need allocating during capture */
+  FD_ERR_WORKSPACE = 5,     /* workspace too small, or would need allocating during capture */
+  FD_ERR_SCRATCH_LIMIT = 6  /* fd_decode_attn_noalloc: the shape needs more than its fixed scratch */
 };
+
+/* Size of the fixed device scratch array behind fd_decode_attn_noalloc. */
+#define FD_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /* Bits of the device error word (fd_get_device_error). */
 enum {
@@ -169,6 +173,33 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
                       const void* v_cache, void* out, const int* lens, int B, int NH,
                       int NKV, int HS, int capacity, int window, float scale,
                       fd_stream_t stream);
+
+/*
+ * fd_decode_attn_noalloc: the same computation as fd_decode_attn, for callers
+ * that must not allocate device memory while they run (for example an op
+ * inside a serving framework whose memory pool owns the device, or a
+ * latency-critical decode loop in which cudaMalloc could synchronise the
+ * device or fail mid-step). It allocates nothing: the split partials live in
+ * a fixed file-scope device array of FD_NOALLOC_SCRATCH_BYTES (32 MiB) that
+ * every device using the library holds until the process exits. There is no
+ * counterpart on the pages; it is an addition of this library.
+ *   - Same arguments, layouts and conventions as fd_decode_attn; the plan is
+ *     made for the current device with max_len <= 0.
+ *   - A shape whose plan needs more than FD_NOALLOC_SCRATCH_BYTES of
+ *     workspace is rejected with FD_ERR_SCRATCH_LIMIT before anything is
+ *     launched (fd_plan + fd_workspace_bytes tell in advance).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress) and caches it; make that first call before
+ *     any stream capture.
+ *   - All calls on a device share the one array and each finds the previous
+ *     call's contents in it (nothing there needs to start at zero). Calls that
+ *     overlap on the GPU - other streams, other threads - race on it: the
+ *     caller must serialise them.
+ * Errors: every FD_ERR_* code.
+ */
+int fd_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out,
+                           const int* lens, int B, int NH, int NKV, int HS, int capacity,
+                           int window, float scale, fd_stream_t stream);
 
 /*
  * fd_get_device_error: wait for `stream`, then return in *err the OR of the
