@@ -276,8 +276,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from decode_attention_04_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from decode_attention_04_gb300.inputs import PROFILE_WORKLOADS, WORKLOADS
+    w = WORKLOADS[args.workload] if args.workload in WORKLOADS else PROFILE_WORKLOADS[args.workload]
 
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
@@ -347,7 +347,7 @@ def main():
             geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak)
 
     traffic = None
-    tf = ROOT / "profiles" / "traffic.json"
+    tf = ROOT / "profiles" / "traffic.txt"
     if tf.exists():
         try:
             traffic = json.loads(tf.read_text()).get(w.name)

@@ -302,25 +302,38 @@ size_t simt_smem_bytes(int G, int HS) {
 
 // ===================================================== tensor-core split kernel
 
-template <int HS_, int NT_, int T_, int NWC_, int NSTAGE_>
+// Shared-memory staging of a tile. The K (and V) rows of a tile arrive as NG
+// groups of R consecutive positions, about 1 KB per group, so one bulk copy
+// moves a whole group: the copy engine's cost is per copy, and 256-byte or
+// 512-byte row copies left it, not HBM, as the limit. Groups are 16 bytes
+// apart beyond their R rows. Row i of group g holds tile position g*R + i.
+//
+// The MMAs walk the tile in a permuted order: MMA row m takes group m % NG,
+// row m / NG. Eight consecutive MMA rows then sit in eight different groups,
+// i.e. in eight different 16-byte bank groups, so every 8-row ldmatrix is
+// conflict-free. Scores, P and the P.V contraction all use the same order;
+// the softmax does not depend on the order of positions.
+template <int HS_, int NT_, int NWC_, int NSTAGE_>
 struct TcCfg {
   static constexpr int HS = HS_;
   static constexpr int NT = NT_;          // 8-row tiles of query rows (G <= 8 * NT)
   static constexpr int NP = 8 * NT;       // padded query rows
-  static constexpr int T = T_;            // positions per pipeline tile
   static constexpr int NWC = NWC_;        // consumer warps
   static constexpr int NSTAGE = NSTAGE_;  // shared-memory ring depth
+  static constexpr int ROWB = HS * 2;     // bytes of one cache row
+  static constexpr int R = ROWB >= 1024 ? 1 : 1024 / ROWB;  // rows per group
+  static constexpr int NG = 16;           // groups per tile
+  static constexpr int T = NG * R;        // positions per pipeline tile
+  static constexpr int GP = R * ROWB + 16;  // group pitch, bytes
   static constexpr int THREADS = (NWC + 1) * 32;
   static constexpr int CTHREADS = NWC * 32;
-  static constexpr int PITCH = HS + 8;    // staged row pitch (bf16); +16 B keeps ldmatrix conflict-free
-  static constexpr int ROWB = HS * 2;     // bytes of one cache row
   static constexpr int DW = HS / NWC;     // head dims owned by one consumer warp
   static constexpr int KD = DW / 16;      // 16-dim steps per warp
-  static constexpr int MP = T / 16;       // 16-position tiles per pipeline tile
+  static constexpr int MP = T / 16;       // 16-row MMA tiles per pipeline tile
   static constexpr int PPITCH = T + 8;    // P row pitch (bf16)
   static constexpr int TPR = CTHREADS / NP;  // softmax threads per query row
   static constexpr int PPT = T / TPR;        // positions per softmax thread
-  static constexpr size_t STAGE_BYTES = static_cast<size_t>(T) * PITCH * 2;
+  static constexpr size_t STAGE_BYTES = static_cast<size_t>(NG) * GP;
   static constexpr size_t OFF_K = 0;
   static constexpr size_t OFF_V = OFF_K + NSTAGE * STAGE_BYTES;
   static constexpr size_t OFF_S = OFF_V + NSTAGE * STAGE_BYTES;              // f32 [NWC][T][NP]
@@ -328,10 +341,21 @@ struct TcCfg {
   static constexpr size_t OFF_A = OFF_P + static_cast<size_t>(2) * NP * PPITCH * 2;  // f32 alpha,m,l [NP]
   static constexpr size_t OFF_BAR = (OFF_A + 3 * NP * 4 + 7) / 8 * 8;        // u64 full[], empty[]
   static constexpr size_t SMEM = OFF_BAR + 2 * NSTAGE * 8;
+
+  // tile position held by MMA row m, and its byte offset in a stage
+  __device__ static __forceinline__ int pos_of(int m) { return (m % NG) * R + m / NG; }
+  __device__ static __forceinline__ int off_of(int m) { return (m % NG) * GP + (m / NG) * ROWB; }
+  // byte offset of tile position j in a stage
+  __device__ static __forceinline__ int off_pos(int j) { return (j / R) * GP + (j % R) * ROWB; }
+  // smallest tile position among MMA rows [16 mt, 16 mt + 16)
+  __device__ static __forceinline__ int min_pos(int mt) { return pos_of(16 * mt); }
+
   static_assert(HS % (16 * NWC) == 0, "head dims must split into 16-wide slices per warp");
+  static_assert(NG % 8 == 0, "eight consecutive MMA rows must fall in eight groups");
   static_assert(T % 16 == 0 && T % TPR == 0, "tile must be whole 16-position MMA tiles");
   static_assert(TPR <= 32 && 32 % TPR == 0, "a row's softmax threads must sit in one warp");
-  static_assert(ROWB % 16 == 0 && (PITCH * 2) % 16 == 0, "bulk copies need 16-byte rows");
+  static_assert(ROWB % 16 == 0 && GP % 16 == 0, "bulk copies need 16-byte granules");
+  static_assert(NG <= 32, "one producer lane per group");
 };
 
 template <class C>
@@ -342,8 +366,6 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hbase = kvh * G;
 
-  uint16_t* sK = reinterpret_cast<uint16_t*>(smem + C::OFF_K);
-  uint16_t* sV = reinterpret_cast<uint16_t*>(smem + C::OFF_V);
   float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
   uint16_t* sP = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
   float* sAlpha = reinterpret_cast<float*>(smem + C::OFF_A);
@@ -402,16 +424,29 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       const int st = i % C::NSTAGE;
       if (i >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((i / C::NSTAGE) - 1) & 1, failed);
       const int nv = min(C::T, n - i * C::T);
-      const int mine = lane < nv ? (nv - lane + 31) / 32 : 0;
-      const uint32_t fb = full0 + 8 * st;
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(mine) * 2u * C::ROWB);
       const long long pbase = p0 + static_cast<long long>(i) * C::T;
-      const uint32_t dk = smem_u32(sK + static_cast<size_t>(st) * C::T * C::PITCH);
-      const uint32_t dv = smem_u32(sV + static_cast<size_t>(st) * C::T * C::PITCH);
-      for (int j = lane; j < nv; j += 32) {
-        const size_t slot = static_cast<size_t>((pbase + j) % a.capacity);
-        bulk_g2s(dk + j * C::PITCH * 2, kb + slot * C::HS, C::ROWB, fb);
-        bulk_g2s(dv + j * C::PITCH * 2, vb + slot * C::HS, C::ROWB, fb);
+      const uint32_t dk = smem_u32(smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES);
+      const uint32_t dv = smem_u32(smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES);
+      const uint32_t fb = full0 + 8 * st;
+      // lane g copies group g: rows [g*R, g*R + rows) of the tile
+      const int g = lane;
+      const int j0 = g * C::R;
+      const int rows = (g < C::NG && j0 < nv) ? min(C::R, nv - j0) : 0;
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * 2u * C::ROWB);
+      if (rows > 0) {
+        const long long pos0 = pbase + j0;
+        const size_t slot0 = static_cast<size_t>(pos0 % a.capacity);
+        const uint32_t goff = static_cast<uint32_t>(g) * C::GP;
+        if (rows == C::R && slot0 + C::R <= static_cast<size_t>(a.capacity)) {
+          bulk_g2s(dk + goff, kb + slot0 * C::HS, C::R * C::ROWB, fb);
+          bulk_g2s(dv + goff, vb + slot0 * C::HS, C::R * C::ROWB, fb);
+        } else {  // a partial group, or one that wraps around the ring: row by row
+          for (int r = 0; r < rows; ++r) {
+            const size_t slot = static_cast<size_t>((pos0 + r) % a.capacity);
+            bulk_g2s(dk + goff + r * C::ROWB, kb + slot * C::HS, C::ROWB, fb);
+            bulk_g2s(dv + goff + r * C::ROWB, vb + slot * C::HS, C::ROWB, fb);
+          }
+        }
       }
     }
     return;
@@ -458,16 +493,15 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % C::NSTAGE;
     mbar_wait(full0 + 8 * st, (i / C::NSTAGE) & 1, failed);
-    const int nv = min(C::T, n - i * C::T);
-    const int nv16 = (nv + 15) & ~15;
-    const uint16_t* tK = sK + static_cast<size_t>(st) * C::T * C::PITCH;
-    uint16_t* tV = sV + static_cast<size_t>(st) * C::T * C::PITCH;
+    const int nv = min(C::T, n - i * C::T);  // valid tile positions: [0, nv)
+    const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES;
+    unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
 
-    // ---- scores: S^T[pos][row] partial over this warp's dims
+    // ---- scores: S^T[m][row] partial over this warp's dims (m = MMA row order)
     float* myS = sS + static_cast<size_t>(warp) * C::T * C::NP;
 #pragma unroll
     for (int mt = 0; mt < C::MP; ++mt) {
-      if (mt * 16 < nv) {
+      if (C::min_pos(mt) < nv) {
         float acc[C::NT][4];
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt)
@@ -475,11 +509,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < C::KD; ++ks) {
-          // matrices: (pos 0-7, d 0-7), (pos 8-15, d 0-7), (pos 0-7, d 8-15), (pos 8-15, d 8-15)
-          const int prow = mt * 16 + lrow + (lmat & 1) * 8;
+          // matrices: (rows 0-7, d 0-7), (rows 8-15, d 0-7), (rows 0-7, d 8-15), (rows 8-15, d 8-15)
+          const int m = mt * 16 + lrow + (lmat & 1) * 8;
           const int dcol = dbase + ks * 16 + (lmat >> 1) * 8;
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(smem_u32(tK + prow * C::PITCH + dcol), a0, a1, a2, a3);
+          ldsm_x4(smem_u32(tK + C::off_of(m) + dcol * 2), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < C::NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
         }
@@ -502,9 +536,9 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       float tmax = kNegInf;
 #pragma unroll
       for (int t = 0; t < C::PPT; ++t) {
-        const int j = sj + t * C::TPR;
+        const int j = sj + t * C::TPR;  // MMA row
         float x = kNegInf;
-        if (j < nv) {
+        if (C::pos_of(j) < nv) {
           float acc = 0.f;
 #pragma unroll
           for (int w = 0; w < C::NWC; ++w) acc += sS[(static_cast<size_t>(w) * C::T + j) * C::NP + sr];
@@ -540,13 +574,13 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       m_run = m_new;
       if (sj == 0) sAlpha[sr] = alpha;
     }
-    // rows [nv, nv16) of the V stage were not written by this tile's copies:
+    // V rows of positions [nv, T) were not written by this tile's copies:
     // zero them so 0-weight positions contribute exactly 0.
-    if (nv < nv16) {
-      const int words = (nv16 - nv) * (C::HS / 8);  // 16-byte words
+    if (nv < C::T) {
+      const int words = (C::T - nv) * (C::HS / 8);  // 16-byte words
       for (int w16 = tid; w16 < words; w16 += C::CTHREADS) {
-        const int r = nv + w16 / (C::HS / 8), c = (w16 % (C::HS / 8)) * 8;
-        *reinterpret_cast<uint4*>(tV + r * C::PITCH + c) = make_uint4(0, 0, 0, 0);
+        const int r = nv + w16 / (C::HS / 8), c = (w16 % (C::HS / 8)) * 16;
+        *reinterpret_cast<uint4*>(tV + C::off_pos(r) + c) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();  // order before the next bulk copies into this stage
     }
@@ -566,7 +600,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
 #pragma unroll
     for (int kp = 0; kp < C::MP; ++kp) {
-      if (kp * 16 < nv16) {
+      if (C::min_pos(kp) < nv) {
         uint32_t pb[C::NT][4];
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
@@ -576,11 +610,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         }
 #pragma unroll
         for (int mt = 0; mt < C::KD; ++mt) {
-          // V^T fragments: matrices (d 0-7, pos 0-7), (d 8-15, pos 0-7), (d 0-7, pos 8-15), (d 8-15, pos 8-15)
-          const int prow = kp * 16 + lrow + (lmat >> 1) * 8;
+          // V^T fragments: matrices (d 0-7, rows 0-7), (d 8-15, rows 0-7), (d 0-7, rows 8-15), (d 8-15, rows 8-15)
+          const int m = kp * 16 + lrow + (lmat >> 1) * 8;
           const int dcol = dbase + mt * 16 + (lmat & 1) * 8;
           uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(smem_u32(tV + prow * C::PITCH + dcol), v0, v1, v2, v3);
+          ldsm_x4_trans(smem_u32(tV + C::off_of(m) + dcol * 2), v0, v1, v2, v3);
 #pragma unroll
           for (int nt = 0; nt < C::NT; ++nt) {
             mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
@@ -627,10 +661,13 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 // ================================================================ merge kernel
 
 constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;  // splits whose loads one warp issues together
 
 // One block per (32-dim slab, query head, sequence). Lane = dim in the slab,
 // warp w = splits w, w + 8, ...; M = max_s m_s, w_s = 2^(m_s - M),
-// out = sum_s w_s O_s / sum_s w_s l_s.
+// out = sum_s w_s O_s / sum_s w_s l_s. Each warp issues the loads of
+// kMergeBatch splits before using any of them, so a row costs about
+// ns / (8 * kMergeBatch) memory round trips instead of ns / 8.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
   __shared__ float sacc[kMergeWarps][32];
   __shared__ float sl[kMergeWarps];
@@ -643,20 +680,40 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   const int chunk = chunk_of(band, a.num_splits, a.granule);
   const int ns = active_splits(band, chunk);
   const size_t row = static_cast<size_t>(b) * a.NH + h;
-  const float* ml = a.ws_ml + row * a.num_splits * 2;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml + row * a.num_splits * 2);
   const int d = slab * 32 + lane;
 
   float M = kNegInf;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
+  for (int s0 = lane; s0 < ns; s0 += 32 * kMergeBatch) {
+    float mv[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int s = s0 + 32 * u;
+      mv[u] = s < ns ? ml[s].x : kNegInf;
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) M = fmaxf(M, mv[u]);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
   float acc = 0.f, lsum = 0.f;
   const float* ob = a.ws_o + row * a.num_splits * a.HS + d;
-  for (int s = warp; s < ns; s += kMergeWarps) {
-    const float w = exp2f(ml[2 * s] - M);
-    lsum += w * ml[2 * s + 1];
-    acc += w * ob[static_cast<size_t>(s) * a.HS];
+  for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeBatch) {
+    float2 mlv[kMergeBatch];
+    float ov[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int s = s0 + kMergeWarps * u;
+      mlv[u] = s < ns ? ml[s] : make_float2(kNegInf, 0.f);
+      ov[u] = s < ns ? ob[static_cast<size_t>(s) * a.HS] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float w = exp2f(mlv[u].x - M);  // 0 for the padding entries
+      lsum += w * mlv[u].y;
+      acc += w * ov[u];
+    }
   }
   sacc[warp][lane] = acc;
   if (lane == 0) sl[warp] = lsum;
@@ -713,15 +770,16 @@ cudaError_t occupancy_tc(int* ctas) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
 }
 
-// Tile configurations: about 32 KB of K+V per pipeline stage, three stages.
-using Tc64x1 = TcCfg<64, 1, 96, 4, 3>;
-using Tc64x2 = TcCfg<64, 2, 96, 4, 3>;
-using Tc128x1 = TcCfg<128, 1, 48, 4, 3>;
-using Tc128x2 = TcCfg<128, 2, 48, 4, 3>;
-using Tc256x1 = TcCfg<256, 1, 32, 4, 3>;
-using Tc256x2 = TcCfg<256, 2, 32, 4, 3>;
-using Tc512x1 = TcCfg<512, 1, 16, 4, 3>;
-using Tc512x2 = TcCfg<512, 2, 16, 4, 3>;
+// Tile configurations: 16 groups of ~1 KB per tensor per stage (about 33 KB of
+// K+V), three stages; G <= 8 or G <= 16 query rows per group.
+using Tc64x1 = TcCfg<64, 1, 4, 3>;
+using Tc64x2 = TcCfg<64, 2, 4, 3>;
+using Tc128x1 = TcCfg<128, 1, 4, 3>;
+using Tc128x2 = TcCfg<128, 2, 4, 3>;
+using Tc256x1 = TcCfg<256, 1, 4, 3>;
+using Tc256x2 = TcCfg<256, 2, 4, 3>;
+using Tc512x1 = TcCfg<512, 1, 4, 3>;
+using Tc512x2 = TcCfg<512, 2, 4, 3>;
 
 template <template <class> class Fn, class... Args>
 cudaError_t with_tc_cfg(int HS, int G, Args&&... args) {

@@ -68,6 +68,21 @@ WORKLOADS = {
 }
 
 
+# Smaller cases of the same geometries for profiler captures (a few GB on the
+# device at most, live band still larger than the 129 MB L2).
+PROFILE_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("llama_ragged_b4", 4, 32, 8, 128, 32768, 0, ragged_max=32768, seed=1104,
+                 desc="Llama geometry ragged, 4 sequences: 32 Q / 8 KV heads, d128, capacity 32768, len ~ U[1,32768]"),
+        Workload("gemma_mqa_long_b1", 1, 16, 1, 512, 131072, 0, lens=(131072,), seed=1105,
+                 desc="Gemma global MQA long context, 1 sequence: 16 Q / 1 KV head, d512, len 131072"),
+        Workload("gemma_local_ring_b16", 16, 16, 8, 256, 1024, 1024, lens=(32768,) * 16, seed=1106,
+                 desc="Gemma local sliding ring, 16 sequences: 16 Q / 8 KV heads, d256, window = capacity = 1024"),
+    ]
+}
+
+
 def draw_lens(w: Workload) -> torch.Tensor:
     """Per-sequence lengths (int32, CPU). Ragged workloads draw U[1, ragged_max]
     from a generator seeded with the workload's seed."""
@@ -139,5 +154,5 @@ def small(w: Workload, **kw) -> Workload:
     return replace(w, **kw)
 
 
-__all__ = ["Workload", "WORKLOADS", "draw_lens", "make_inputs", "live_slots",
+__all__ = ["Workload", "WORKLOADS", "PROFILE_WORKLOADS", "draw_lens", "make_inputs", "live_slots",
            "poison_dead_slots", "small", "BF16_NAN_BITS"]
