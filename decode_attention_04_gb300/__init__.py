@@ -42,10 +42,12 @@ class fd_plan_t(ctypes.Structure):
     _fields_ = [
         ("num_splits", ctypes.c_int),
         ("path", ctypes.c_int),
+        ("cluster", ctypes.c_int),
         ("granule", ctypes.c_int),
         ("max_band", ctypes.c_int),
         ("ctas_per_sm", ctypes.c_int),
         ("num_sms", ctypes.c_int),
+        ("max_cluster", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),
         ("NH", ctypes.c_int),
@@ -82,8 +84,8 @@ def load_library(path: Path | str | None = None):
     planp = ctypes.POINTER(fd_plan_t)
     sig = {
         "fd_plan": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, planp]),
-        "fd_plan_sms": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
-        "fd_plan_override": (ci, [planp, ci, ci]),
+        "fd_plan_sms": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
+        "fd_plan_override": (ci, [planp, ci, ci, ci]),
         "fd_workspace_bytes": (sz, [planp]),
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
@@ -142,15 +144,15 @@ def fd_plan(B, NH, NKV, HS, capacity, window, max_len=0, device=None) -> fd_plan
     return p
 
 
-def fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm) -> fd_plan_t:
+def fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, max_cluster=8) -> fd_plan_t:
     p = fd_plan_t()
     _check(load_library().fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm,
-                                      ctypes.byref(p)), "fd_plan_sms")
+                                      max_cluster, ctypes.byref(p)), "fd_plan_sms")
     return p
 
 
-def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO) -> fd_plan_t:
-    _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path), "fd_plan_override")
+def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO, cluster: int = 0) -> fd_plan_t:
+    _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path, cluster), "fd_plan_override")
     return plan
 
 

@@ -18,7 +18,6 @@
 namespace {
 
 constexpr int kMaxGroup = 16;
-constexpr int kDefaultCtasPerSm = 2;
 
 bool supported_hs(int HS) { return HS == 64 || HS == 128 || HS == 256 || HS == 512; }
 
@@ -35,23 +34,32 @@ int check_shape(int B, int NH, int NKV, int HS, int capacity, int window) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Partial slots per row: one per block, or one per cluster of blocks.
+int slots(const fd_plan_t& p) { return p.num_splits / (p.cluster > 0 ? p.cluster : 1); }
+
 // Bytes of the (O) part of the workspace; the (m, l) part follows it.
 size_t ws_o_bytes(const fd_plan_t& p) {
-  return round_up(static_cast<size_t>(p.B) * p.NH * p.num_splits * p.HS * sizeof(float), 256);
+  return round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * p.HS * sizeof(float), 256);
 }
 
 size_t ws_total(const fd_plan_t& p) {
-  if (p.num_splits <= 1) return 0;
-  return ws_o_bytes(p) + round_up(static_cast<size_t>(p.B) * p.NH * p.num_splits * 2 * sizeof(float), 256);
+  if (slots(p) <= 1) return 0;
+  return ws_o_bytes(p) + round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * 2 * sizeof(float), 256);
+}
+
+bool valid_cluster(int cluster, int num_splits, int HS, int path) {
+  if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
+  if (num_splits % cluster != 0 || (HS / cluster) % 4 != 0) return false;
+  return cluster == 1 || path == FD_PATH_TC;
 }
 
 // The split rule, documented in fd_decode_attn.h beside fd_plan_t.
 int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
-              int ctas_per_sm, int path, fd_plan_t* plan) {
+              int ctas_per_sm, int max_cluster, int path, fd_plan_t* plan) {
   if (!plan) return FD_ERR_INVALID_ARG;
   int rc = check_shape(B, NH, NKV, HS, capacity, window);
   if (rc != FD_OK) return rc;
-  if (num_sms <= 0 || ctas_per_sm <= 0) return FD_ERR_INVALID_ARG;
+  if (num_sms <= 0 || ctas_per_sm <= 0 || max_cluster < 1) return FD_ERR_INVALID_ARG;
   if (path == FD_PATH_AUTO) path = FD_PATH_TC;
   if (path != FD_PATH_TC && path != FD_PATH_SIMT) return FD_ERR_INVALID_ARG;
 
@@ -62,7 +70,11 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
 
   const int granule = fd::plan_granule(path, HS);
   const long long units = static_cast<long long>(B > 0 ? B : 1) * NKV;
-  const long long slots = static_cast<long long>(num_sms) * ctas_per_sm;
+  // With large query groups a partial (G x HS floats) is costly next to a
+  // split's K/V bytes, so fill each SM once rather than with every resident
+  // block.
+  const int G = NH / NKV;
+  const long long slots = static_cast<long long>(num_sms) * (G >= 8 ? 1 : ctas_per_sm);
   long long s_fill = (slots + units - 1) / units;
   if (s_fill < 1) s_fill = 1;
   auto chunk_for = [&](long long S) {
@@ -84,9 +96,17 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   if (S < 1) S = 1;
   if (S > 65535 * 64) S = 65535 * 64;
 
+  // No clusters by default: a cluster must find `cluster` free block slots in
+  // one GPC at once, and on GB300 that stranded slots and cost more than the
+  // smaller partials saved (measured on every workload here). Clusters remain
+  // available through fd_plan_override.
+  const int cluster = 1;
+
   fd_plan_t p{};
   p.num_splits = static_cast<int>(S);
   p.path = path;
+  p.cluster = cluster;
+  p.max_cluster = max_cluster;
   p.granule = granule;
   p.max_band = max_band;
   p.ctas_per_sm = ctas_per_sm;
@@ -189,6 +209,7 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.capacity = plan.capacity;
   a.window = plan.window;
   a.num_splits = plan.num_splits;
+  a.cluster = plan.cluster;
   a.granule = plan.granule;
   a.path = plan.path;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -200,8 +221,9 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
 extern "C" {
 
 int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
-                int ctas_per_sm, fd_plan_t* plan) {
-  return make_plan(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, FD_PATH_AUTO, plan);
+                int ctas_per_sm, int max_cluster, fd_plan_t* plan) {
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, max_cluster, FD_PATH_AUTO,
+                   plan);
 }
 
 int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int device,
@@ -215,27 +237,30 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
   int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess) return FD_ERR_CUDA;
   if (prev != device && cudaSetDevice(device) != cudaSuccess) return FD_ERR_CUDA;
-  int ctas = 0;
+  int ctas = 0, max_cluster = 1;
   cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, NH / NKV, &ctas);
+  if (e == cudaSuccess) e = fd::query_max_cluster(HS, NH / NKV, &max_cluster);
   if (prev != device) cudaSetDevice(prev);
   if (e != cudaSuccess || ctas <= 0) return FD_ERR_CUDA;
-  return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, FD_PATH_AUTO, plan);
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, max_cluster, FD_PATH_AUTO, plan);
 }
 
-int fd_plan_override(fd_plan_t* plan, int num_splits, int path) {
-  if (!plan || num_splits < 0) return FD_ERR_INVALID_ARG;
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster) {
+  if (!plan || num_splits < 0 || cluster < 0 || num_splits > 65535 * 64) return FD_ERR_INVALID_ARG;
   if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_TC) return FD_ERR_INVALID_ARG;
   if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
     return FD_ERR_INVALID_ARG;
+  fd_plan_t p = *plan;
   if (path != FD_PATH_AUTO) {
-    plan->path = path;
-    plan->granule = fd::plan_granule(path, plan->HS);
+    p.path = path;
+    p.granule = fd::plan_granule(path, p.HS);
   }
-  if (num_splits > 0) {
-    if (num_splits > 65535 * 64) return FD_ERR_INVALID_ARG;
-    plan->num_splits = num_splits;
-  }
-  plan->workspace_bytes = ws_total(*plan);
+  if (num_splits > 0) p.num_splits = num_splits;
+  if (cluster > 0) p.cluster = cluster;
+  if (p.path == FD_PATH_SIMT && cluster == 0) p.cluster = 1;  // the SIMT path has no clusters
+  if (!valid_cluster(p.cluster, p.num_splits, p.HS, p.path)) return FD_ERR_INVALID_ARG;
+  p.workspace_bytes = ws_total(p);
+  *plan = p;
   return FD_OK;
 }
 
@@ -251,7 +276,8 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
   if (plan->B != B || plan->NH != NH || plan->NKV != NKV || plan->HS != HS || plan->capacity != capacity ||
       plan->window != window)
     return FD_ERR_INVALID_ARG;
-  if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1)
+  if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1 ||
+      !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path))
     return FD_ERR_INVALID_ARG;
   return run(*plan, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens, scale,
              reinterpret_cast<cudaStream_t>(stream));

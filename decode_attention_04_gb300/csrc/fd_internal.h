@@ -22,6 +22,7 @@ struct LaunchArgs {
   float* ws_ml;             // fp32 [B][NH][S][2]   (m in log2 units, l)
   int B, NH, NKV, HS, capacity, window;  // window <= 0: none
   int num_splits;           // S
+  int cluster;              // blocks per cluster along the splits (S % cluster == 0)
   int granule;              // chunk rounding, positions
   int path;                 // FD_PATH_SIMT / FD_PATH_TC
   float scale_log2;         // scale * log2(e)
@@ -34,6 +35,10 @@ int plan_granule(int path, int HS);
 
 // Resident CTAs per SM of the kernel a plan would launch (occupancy query).
 cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas);
+
+// Largest cluster size (16, 8, ... 1) of the tensor-core split kernel that the
+// device can schedule (cluster occupancy query).
+cudaError_t query_max_cluster(int HS, int G, int* cluster);
 
 // Launch the split kernel (and the merge kernel when S > 1) on `stream`.
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);

@@ -160,6 +160,44 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Thread-block clusters: rank of this block in its cluster, another block's
+// shared-memory address, loads through distributed shared memory, and a
+// barrier over every thread of the cluster (release/acquire, so shared-memory
+// writes before it are visible to the whole cluster after it).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -303,10 +341,11 @@ size_t simt_smem_bytes(int G, int HS) {
 // ===================================================== tensor-core split kernel
 
 // Shared-memory staging of a tile. The K (and V) rows of a tile arrive as NG
-// groups of R consecutive positions, about 1 KB per group, so one bulk copy
-// moves a whole group: the copy engine's cost is per copy, and 256-byte or
-// 512-byte row copies left it, not HBM, as the limit. Groups are 16 bytes
-// apart beyond their R rows. Row i of group g holds tile position g*R + i.
+// groups of R consecutive positions, 2 KB per group, so one bulk copy moves a
+// whole group: a block's copy rate is set by the number of copies it issues
+// (on GB300, about 15 / 23 / 33 GB/s per block with 0.5 / 1 / 2 KB copies),
+// not by their bytes. Groups are 16 bytes apart beyond their R rows. Row i of
+// group g holds tile position g*R + i.
 //
 // The MMAs walk the tile in a permuted order: MMA row m takes group m % NG,
 // row m / NG. Eight consecutive MMA rows then sit in eight different groups,
@@ -321,8 +360,8 @@ struct TcCfg {
   static constexpr int NWC = NWC_;        // consumer warps
   static constexpr int NSTAGE = NSTAGE_;  // shared-memory ring depth
   static constexpr int ROWB = HS * 2;     // bytes of one cache row
-  static constexpr int R = ROWB >= 1024 ? 1 : 1024 / ROWB;  // rows per group
-  static constexpr int NG = 16;           // groups per tile
+  static constexpr int R = ROWB >= 2048 ? 1 : 2048 / ROWB;  // rows per group
+  static constexpr int NG = 8;            // groups per tile
   static constexpr int T = NG * R;        // positions per pipeline tile
   static constexpr int GP = R * ROWB + 16;  // group pitch, bytes
   static constexpr int THREADS = (NWC + 1) * 32;
@@ -356,6 +395,9 @@ struct TcCfg {
   static_assert(TPR <= 32 && 32 % TPR == 0, "a row's softmax threads must sit in one warp");
   static_assert(ROWB % 16 == 0 && GP % 16 == 0, "bulk copies need 16-byte granules");
   static_assert(NG <= 32, "one producer lane per group");
+  // cluster reduction: O parked in the K stages, weights in the score buffer
+  static_assert(static_cast<size_t>(NP) * HS * 4 <= NSTAGE * STAGE_BYTES, "O must fit the K stages");
+  static_assert(NP * 16 + 2 * NP <= NWC * T * NP, "cluster weights must fit the score buffer");
 };
 
 template <class C>
@@ -398,9 +440,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int chunk = chunk_of(band, a.num_splits, a.granule);
   const long long p0 = lo + static_cast<long long>(s) * chunk;
   const long long p1 = min(static_cast<long long>(lo) + band, p0 + chunk);
-  const bool direct = a.num_splits == 1;
+  const int CS = a.cluster;                 // blocks per cluster along the splits
+  const bool direct = a.num_splits == CS;   // one block / cluster spans every split
+  const int n = p0 < p1 ? static_cast<int>(p1 - p0) : 0;
 
-  if (p0 >= p1) {
+  if (n == 0 && CS == 1) {
     if (direct) {  // len == 0: the output row is zero
       for (int i = tid; i < G * C::HS; i += C::THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / C::HS) * C::HS + i % C::HS;
@@ -410,9 +454,22 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
     return;
   }
-  const int n = static_cast<int>(p1 - p0);
+  // In a cluster every block, even one with an empty slice (m = -inf, l = 0,
+  // O = 0), takes part in the reduction at the end.
   const int ntiles = (n + C::T - 1) / C::T;
   __syncthreads();
+
+  const int grp = lane >> 2, t4 = lane & 3;
+  const int dbase = warp * C::DW;
+  float o[C::KD][C::NT][4];
+#pragma unroll
+  for (int mt = 0; mt < C::KD; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+  // softmax role: row sr, MMA rows sj + TPR * t
+  const int sr = tid / C::TPR, sj = tid % C::TPR;
 
   if (warp == C::NWC) {
     // ------------------------------------------------------------ producer
@@ -449,12 +506,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         }
       }
     }
-    return;
-  }
-
+  } else {
   // -------------------------------------------------------------- consumers
-  const int grp = lane >> 2, t4 = lane & 3;
-  const int dbase = warp * C::DW;
 
   // Q^T as MMA B fragments for this warp's dims: b0 = (dims 2t4..2t4+1, row grp),
   // b1 = (dims 8+2t4.., row grp) of each 16-dim step.
@@ -474,16 +527,6 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       qf[ks][nt][1] = x1;
     }
 
-  float o[C::KD][C::NT][4];
-#pragma unroll
-  for (int mt = 0; mt < C::KD; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < C::NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-
-  // softmax role: row sr, positions sj + TPR * t
-  const int sr = tid / C::TPR, sj = tid % C::TPR;
   float m_run = kNegInf, l_run = 0.f;
 
   // ldmatrix lane addressing
@@ -627,35 +670,120 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
   }
 
-  // ---- epilogue: partial (O, m, l) or, with one split, the normalised row
-  if (sr < G && sj == 0) {
-    sM[sr] = m_run;
-    sL[sr] = l_run;
+    if (sr < G && sj == 0) {
+      sM[sr] = m_run;
+      sL[sr] = l_run;
+    }
+    named_bar_sync(1, C::CTHREADS);  // every consumer is past its last tile
   }
-  named_bar_sync(1, C::CTHREADS);
+
+  if (CS == 1) {
+    // ---- one block per slice: its partial (O, m, l), or with one split the
+    // normalised row
+    if (warp == C::NWC) return;
 #pragma unroll
-  for (int mt = 0; mt < C::KD; ++mt)
+    for (int mt = 0; mt < C::KD; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < C::NT; ++nt)
+      for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = nt * 8 + 2 * t4 + (e & 1);
-        if (r >= G) continue;
-        const int d = dbase + mt * 16 + grp + (e >> 1) * 8;
-        const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
-        if (direct) {
-          const float val = o[mt][nt][e] / sL[r];
-          a.out[row * C::HS + d] = f32_to_bf16_bits(val);
-          if (a.out_f32) a.out_f32[row * C::HS + d] = val;
-        } else {
-          a.ws_o[(row * a.num_splits + s) * C::HS + d] = o[mt][nt][e];
+        for (int e = 0; e < 4; ++e) {
+          const int r = nt * 8 + 2 * t4 + (e & 1);
+          if (r >= G) continue;
+          const int d = dbase + mt * 16 + grp + (e >> 1) * 8;
+          const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
+          if (direct) {
+            const float val = o[mt][nt][e] / sL[r];
+            a.out[row * C::HS + d] = f32_to_bf16_bits(val);
+            if (a.out_f32) a.out_f32[row * C::HS + d] = val;
+          } else {
+            a.ws_o[(row * a.num_splits + s) * C::HS + d] = o[mt][nt][e];
+          }
         }
-      }
-  if (!direct && tid < G) {
-    const size_t r = ((static_cast<size_t>(b) * a.NH + hbase + tid) * a.num_splits + s) * 2;
-    a.ws_ml[r] = sM[tid];
-    a.ws_ml[r + 1] = sL[tid];
+    if (!direct && tid < G) {
+      const size_t r = ((static_cast<size_t>(b) * a.NH + hbase + tid) * a.num_splits + s) * 2;
+      a.ws_ml[r] = sM[tid];
+      a.ws_ml[r + 1] = sL[tid];
+    }
+    return;
   }
+
+  // ---- cluster reduction through distributed shared memory. Each block parks
+  // its unnormalised O (rows < G, fp32 [G][HS]) in its now idle K stages; after
+  // a cluster barrier, block `rank` combines head dims
+  // [rank * HS / CS, (rank + 1) * HS / CS) of every row over the CS blocks:
+  // M = max_c m_c, w_c = 2^(m_c - M), O = sum_c w_c O_c, L = sum_c w_c l_c.
+  float* sO = reinterpret_cast<float*>(smem + C::OFF_K);
+  if (warp != C::NWC) {
+#pragma unroll
+    for (int mt = 0; mt < C::KD; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = nt * 8 + 2 * t4 + (e & 1);
+          if (r < G) sO[r * C::HS + dbase + mt * 16 + grp + (e >> 1) * 8] = o[mt][nt][e];
+        }
+  }
+  cluster_sync_all();
+
+  const uint32_t rank = cluster_ctarank();
+  float* sW = sS;                 // [G][CS] weights
+  float* sMt = sS + G * CS;       // [G] combined max
+  float* sLt = sMt + G;           // [G] combined sum
+  if (tid < G) {
+    float M = kNegInf;
+    for (int c = 0; c < CS; ++c) M = fmaxf(M, ld_dsmem(map_to_rank(smem_u32(sM + tid), c)));
+    float L = 0.f;
+    for (int c = 0; c < CS; ++c) {
+      const float mc = ld_dsmem(map_to_rank(smem_u32(sM + tid), c));
+      const float lc = ld_dsmem(map_to_rank(smem_u32(sL + tid), c));
+      const float w = (M == kNegInf) ? 0.f : exp2f(mc - M);
+      sW[tid * CS + c] = w;
+      L += w * lc;
+    }
+    sMt[tid] = M;
+    sLt[tid] = L;
+  }
+  __syncthreads();
+
+  const int dc4 = C::HS / CS / 4;  // float4 columns per block
+  const int q = s / CS;            // this cluster's partial slot
+  const int nq = a.num_splits / CS;
+  for (int it = tid; it < G * dc4; it += C::THREADS) {
+    const int r = it / dc4;
+    const int d = static_cast<int>(rank) * (C::HS / CS) + (it % dc4) * 4;
+    const uint32_t src = smem_u32(sO + r * C::HS + d);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < CS; ++c) {
+      const float w = sW[r * CS + c];
+      const float4 v = ld_dsmem4(map_to_rank(src, c));
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
+    if (direct) {
+      const float L = sLt[r];
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float4 val = (L > 0.f || isnan(L)) ? make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L)
+                                               : make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+      const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+      *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+    } else {
+      *reinterpret_cast<float4*>(a.ws_o + (row * nq + q) * C::HS + d) = acc;
+    }
+  }
+  if (!direct && rank == 0 && tid < G) {
+    const size_t r = ((static_cast<size_t>(b) * a.NH + hbase + tid) * nq + q) * 2;
+    a.ws_ml[r] = sMt[tid];
+    a.ws_ml[r + 1] = sLt[tid];
+  }
+  cluster_sync_all();  // no block leaves while another still reads its shared memory
 }
 
 // ================================================================ merge kernel
@@ -664,13 +792,13 @@ constexpr int kMergeWarps = 8;
 constexpr int kMergeBatch = 8;  // splits whose loads one warp issues together
 
 // One block per (32-dim slab, query head, sequence). Lane = dim in the slab,
-// warp w = splits w, w + 8, ...; M = max_s m_s, w_s = 2^(m_s - M),
+// warp w = partials w, w + 8, ...; M = max_s m_s, w_s = 2^(m_s - M),
 // out = sum_s w_s O_s / sum_s w_s l_s. Each warp issues the loads of
-// kMergeBatch splits before using any of them, so a row costs about
-// ns / (8 * kMergeBatch) memory round trips instead of ns / 8.
+// kMergeBatch partials before using any of them.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
   __shared__ float sacc[kMergeWarps][32];
   __shared__ float sl[kMergeWarps];
+  __shared__ float sm[kMergeWarps];
   const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();
@@ -678,27 +806,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, false, &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
-  const int ns = active_splits(band, chunk);
+  // one partial per block (cluster size 1) or per cluster of CS blocks
+  const int CS = a.cluster;
+  const int nslots = a.num_splits / CS;
+  const int ns = (active_splits(band, chunk) + CS - 1) / CS;
   const size_t row = static_cast<size_t>(b) * a.NH + h;
-  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml + row * a.num_splits * 2);
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml + row * nslots * 2);
   const int d = slab * 32 + lane;
 
-  float M = kNegInf;
-  for (int s0 = lane; s0 < ns; s0 += 32 * kMergeBatch) {
-    float mv[kMergeBatch];
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + 32 * u;
-      mv[u] = s < ns ? ml[s].x : kNegInf;
-    }
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) M = fmaxf(M, mv[u]);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-
-  float acc = 0.f, lsum = 0.f;
-  const float* ob = a.ws_o + row * a.num_splits * a.HS + d;
+  // Each warp folds its splits into a running (max, sum, O) with one rescale
+  // per batch, so the whole row costs one memory round trip per batch; the
+  // eight warp results are then combined the same way.
+  float mw = kNegInf, lw = 0.f, acc = 0.f;
+  const float* ob = a.ws_o + row * nslots * a.HS + d;
   for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeBatch) {
     float2 mlv[kMergeBatch];
     float ov[kMergeBatch];
@@ -708,22 +828,40 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
       mlv[u] = s < ns ? ml[s] : make_float2(kNegInf, 0.f);
       ov[u] = s < ns ? ob[static_cast<size_t>(s) * a.HS] : 0.f;
     }
+    float bm = kNegInf;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) bm = fmaxf(bm, mlv[u].x);
+    const float mn = fmaxf(mw, bm);
+    if (mn == kNegInf) continue;  // nothing but padding
+    const float sc = exp2f(mw - mn);  // 0 while mw is still -inf
+    lw *= sc;
+    acc *= sc;
 #pragma unroll
     for (int u = 0; u < kMergeBatch; ++u) {
-      const float w = exp2f(mlv[u].x - M);  // 0 for the padding entries
-      lsum += w * mlv[u].y;
+      const float w = exp2f(mlv[u].x - mn);  // 0 for padding
+      lw += w * mlv[u].y;
       acc += w * ov[u];
     }
+    mw = mn;
   }
   sacc[warp][lane] = acc;
-  if (lane == 0) sl[warp] = lsum;
+  if (lane == 0) {
+    sl[warp] = lw;
+    sm[warp] = mw;
+  }
   __syncthreads();
   if (warp == 0) {
-    float t = 0.f, L = 0.f;
+    float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) {
-      t += sacc[w][lane];
-      L += sl[w];
+    for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, sm[w]);
+    float t = 0.f, L = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < kMergeWarps; ++w) {
+        const float c = exp2f(sm[w] - M);
+        t += c * sacc[w][lane];
+        L += c * sl[w];
+      }
     }
     const float val = ns > 0 ? t / L : 0.f;
     a.out[row * a.HS + d] = f32_to_bf16_bits(val);
@@ -738,17 +876,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
 // kernels above wait (griddepcontrol.wait) before touching any input.
 template <class... KArgs, class... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
+                       int cluster, Args&&... args) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -758,8 +903,12 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
+  if (a.cluster > 8) {
+    e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(a.num_splits, a.NKV, a.B);
-  return launch_pdl(split_tc_kernel<C>, grid, dim3(C::THREADS), C::SMEM, stream, a);
+  return launch_pdl(split_tc_kernel<C>, grid, dim3(C::THREADS), C::SMEM, stream, a.cluster, a);
 }
 
 template <class C>
@@ -770,7 +919,7 @@ cudaError_t occupancy_tc(int* ctas) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
 }
 
-// Tile configurations: 16 groups of ~1 KB per tensor per stage (about 33 KB of
+// Tile configurations: 8 groups of 2 KB per tensor per stage (about 33 KB of
 // K+V), three stages; G <= 8 or G <= 16 query rows per group.
 using Tc64x1 = TcCfg<64, 1, 4, 3>;
 using Tc64x2 = TcCfg<64, 2, 4, 3>;
@@ -792,6 +941,42 @@ cudaError_t with_tc_cfg(int HS, int G, Args&&... args) {
     default: return cudaErrorInvalidValue;
   }
 }
+
+template <class C>
+cudaError_t max_cluster_tc(int* cluster) {
+  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const bool nonportable =
+      cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (!nonportable) cudaGetLastError();
+  for (int cs = nonportable ? 16 : 8; cs >= 2; cs /= 2) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(cs, 1, 1);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, split_tc_kernel<C>, &cfg) == cudaSuccess && n > 0) {
+      *cluster = cs;
+      return cudaSuccess;
+    }
+    cudaGetLastError();
+  }
+  *cluster = 1;
+  return cudaSuccess;
+}
+
+template <class C>
+struct MaxClusterFn {
+  static cudaError_t run(int* cluster) { return max_cluster_tc<C>(cluster); }
+};
 
 template <class C>
 struct LaunchFn {
@@ -833,6 +1018,8 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas) {
   return with_tc_cfg<OccFn>(HS, G, ctas);
 }
 
+cudaError_t query_max_cluster(int HS, int G, int* cluster) { return with_tc_cfg<MaxClusterFn>(HS, G, cluster); }
+
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
   const int G = a.NH / a.NKV;
   cudaError_t e;
@@ -841,13 +1028,13 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     dim3 grid(a.num_splits, a.NKV, a.B);
-    e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, a);
+    e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, 1, a);
   } else {
     e = with_tc_cfg<LaunchFn>(a.HS, G, a, stream);
   }
-  if (e != cudaSuccess || a.num_splits == 1) return e;
+  if (e != cudaSuccess || a.num_splits == a.cluster) return e;  // the split kernel wrote the output
   dim3 mgrid(a.HS / 32, a.NH, a.B);
-  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, a);
+  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err) {

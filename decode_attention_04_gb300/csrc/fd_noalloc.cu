@@ -63,7 +63,7 @@ extern "C" int fd_decode_attn_noalloc(const void* q, const void* k_cache, const 
                                       int window, float scale, fd_stream_t stream) {
   fd_plan_t plan;
   // Shape errors first, before any CUDA call (the SM count here is a dummy).
-  int rc = fd_plan_sms(B, NH, NKV, HS, capacity, window, 0, 1, 1, &plan);
+  int rc = fd_plan_sms(B, NH, NKV, HS, capacity, window, 0, 1, 1, 1, &plan);
   if (rc != FD_OK) return rc;
   if (B == 0) return FD_OK;
   if (!q || !k_cache || !v_cache || !out || !lens) return FD_ERR_INVALID_ARG;

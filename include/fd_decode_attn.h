@@ -87,9 +87,10 @@ enum {
 };
 
 /*
- * Launch plan: how many key-sequence splits each (sequence, KV head) gets and
- * how much workspace the split partials need. Built by fd_plan / fd_plan_sms;
- * the caller may change num_splits and path through fd_plan_override only.
+ * Launch plan: how many key-sequence splits each (sequence, KV head) gets,
+ * how the split blocks are grouped into thread-block clusters, and how much
+ * workspace the partials need. Built by fd_plan / fd_plan_sms; the caller may
+ * change num_splits, path and cluster through fd_plan_override only.
  *
  * Split rule (the page gives none; "One KV head breaks the textbook" only says
  * to split the key sequence across blocks so one KV head still fills the GPU):
@@ -97,16 +98,29 @@ enum {
  * the GPU once; a split then never exceeds `max_chunk` positions (a bound that
  * keeps ragged batches balanced), rounding num_splits up to a whole number of
  * waves when that bound applies. On the device each sequence cuts its own band
- * into chunks of ceil(band_b / num_splits) rounded up to `granule` positions,
- * so a short sequence uses fewer, not emptier, splits.
+ * into chunks of ceil(band_b / num_splits) positions, so a short sequence
+ * uses fewer, not emptier, splits.
+ *
+ * With G >= 8 query rows per KV head a partial (G x HS floats) is costly
+ * next to a split's K/V bytes, and the plan fills each SM once instead of
+ * with every resident block.
+ *
+ * Clusters (opt-in through fd_plan_override; plans use cluster = 1): the
+ * blocks of `cluster` consecutive splits form a thread-block cluster and
+ * combine their partials through distributed shared memory, so only
+ * num_splits / cluster partials per row reach the workspace; when
+ * cluster == num_splits one cluster covers the whole band and writes the
+ * output itself (no merge kernel, no workspace).
  */
 typedef struct {
   int num_splits;          /* S: grid splits per (sequence, KV head) */
   int path;                /* FD_PATH_SIMT or FD_PATH_TC */
+  int cluster;             /* blocks per cluster along the splits; divides S; 1 = none */
   int granule;             /* chunk rounding on the device, positions */
   int max_band;            /* band bound the plan was sized for */
   int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
   int num_sms;             /* SM count the plan assumed */
+  int max_cluster;         /* largest cluster the device schedules for this kernel */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
   int B, NH, NKV, HS, capacity, window;
@@ -124,24 +138,28 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
             int device, fd_plan_t* plan);
 
 /*
- * fd_plan_sms: the same plan for a GPU with `num_sms` SMs and `ctas_per_sm`
- * resident CTAs per SM, without touching any device (for tools and tests).
+ * fd_plan_sms: the same plan for a GPU with `num_sms` SMs, `ctas_per_sm`
+ * resident CTAs per SM and clusters of at most `max_cluster` blocks, without
+ * touching any device (for tools and tests).
  */
 int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
-                int num_sms, int ctas_per_sm, fd_plan_t* plan);
+                int num_sms, int ctas_per_sm, int max_cluster, fd_plan_t* plan);
 
 /*
  * fd_plan_override: force the split count (num_splits >= 1; 0 keeps the
- * plan's) and/or the kernel family (path != FD_PATH_AUTO), recomputing
+ * plan's), the kernel family (path != FD_PATH_AUTO) and/or the cluster size
+ * (cluster >= 1, a power of two <= 16 that divides num_splits and HS / 4;
+ * 0 keeps the plan's; the SIMT path takes cluster 1 only), recomputing
  * workspace_bytes. Used to test that the result does not depend on the split
- * count, and to bisect. Errors: FD_ERR_INVALID_ARG.
+ * count or the cluster size, and to bisect. Errors: FD_ERR_INVALID_ARG.
  */
-int fd_plan_override(fd_plan_t* plan, int num_splits, int path);
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster);
 
 /*
- * fd_workspace_bytes: workspace the split partials of a plan need:
- * B * NH * num_splits * (HS + 2) * 4 bytes, rounded up to 256 (0 when
- * num_splits == 1, where the split kernel writes the output itself).
+ * fd_workspace_bytes: workspace the partials of a plan need: with
+ * P = num_splits / cluster partial slots per row, B * NH * P * (HS + 2) * 4
+ * bytes, each part rounded up to 256 (0 when P == 1: the split kernel then
+ * writes the output itself).
  */
 size_t fd_workspace_bytes(const fd_plan_t* plan);
 

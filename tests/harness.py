@@ -43,7 +43,7 @@ class Guarded:
 
 
 def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len: int = 0,
-        poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None):
+        poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None, cluster: int = 0):
     """One fd_decode_attn_ex call. Returns dict with out (bf16, cpu), out32
     (fp32, cpu), plan, deverr, canaries (bool)."""
     dev = torch.device(device)
@@ -52,8 +52,8 @@ def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len:
     else:
         qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len)
-    if splits or path:
-        fd.fd_plan_override(plan, splits, path)
+    if splits or path or cluster:
+        fd.fd_plan_override(plan, splits, path, cluster)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)         # NaN-filled: unwritten rows show up
     o32 = Guarded(n * 4, dev, fill=0xFF)

@@ -66,10 +66,13 @@ def test_plan_fills_the_gpu_and_sizes_workspace(name, lib):
     chunk = -(-band // p.num_splits)
     chunk = -(-chunk // p.granule) * p.granule
     active = -(-band // chunk)
-    # (granule rounding may leave a few percent of the slots idle)
-    assert units * active >= 0.9 * min(152 * 2, units * -(-band // p.granule))
-    expect_ws = 0 if p.num_splits == 1 else (
-        -(-(w.B * w.NH * p.num_splits * w.HS * 4) // 256) * 256 + -(-(w.B * w.NH * p.num_splits * 8) // 256) * 256)
+    # one block per CTA slot (per SM when G >= 8, where partials are costly)
+    per_sm = 1 if w.G >= 8 else 2
+    assert units * active >= 0.9 * min(152 * per_sm, units * -(-band // p.granule))
+    P = p.num_splits // p.cluster
+    assert p.num_splits % p.cluster == 0
+    expect_ws = 0 if P == 1 else (
+        -(-(w.B * w.NH * P * w.HS * 4) // 256) * 256 + -(-(w.B * w.NH * P * 8) // 256) * 256)
     assert p.workspace_bytes == expect_ws == fd.fd_workspace_bytes(p)
     # workspace is bounded by partials, never by the cache allocation
     assert p.workspace_bytes <= 32 << 20
@@ -79,6 +82,12 @@ def test_plan_mqa_one_kv_head_uses_every_sm(lib):
     w = WORKLOADS["gemma_global_mqa_32k"]
     p = _plan(w)
     assert p.num_splits >= 152  # one KV head still spreads over all SMs
+    assert p.cluster == 1  # clusters are opt-in
+
+
+def test_plan_uses_no_clusters_by_default(lib):
+    for name in WORKLOADS:
+        assert _plan(WORKLOADS[name]).cluster == 1
 
 
 def test_plan_max_len_tightens_short_context(lib):
@@ -108,6 +117,17 @@ def test_plan_override(lib):
         fd.fd_plan_override(p, -1, 0)
     with pytest.raises(fd.FdError):
         fd.fd_plan_override(p, 0, 9)
+    # clusters: powers of two <= 16 dividing S (and HS / 4); tensor-core path only
+    fd.fd_plan_override(p, 32, fd.FD_PATH_TC, 8)
+    assert p.cluster == 8 and p.workspace_bytes == fd.fd_workspace_bytes(p) > 0
+    fd.fd_plan_override(p, 16, 0, 16)
+    assert p.cluster == 16 and p.workspace_bytes == 0  # one cluster spans every split
+    for bad in [(24, 0, 16), (32, 0, 3), (32, 0, 32), (32, fd.FD_PATH_SIMT, 8)]:
+        q = fd.fd_plan_t.from_buffer_copy(p)
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_override(q, *bad)
+    fd.fd_plan_override(p, 5, fd.FD_PATH_SIMT, 1)
+    assert p.cluster == 1 and p.path == fd.FD_PATH_SIMT
 
 
 @pytest.mark.parametrize("args,code", [
@@ -122,7 +142,7 @@ def test_plan_override(lib):
 def test_shape_errors_before_any_cuda_call(lib, args, code):
     B, NH, NKV, HS, cap, win = args
     p = fd.fd_plan_t()
-    assert lib.fd_plan_sms(B, NH, NKV, HS, cap, win, 0, 152, 2, ctypes.byref(p)) == code
+    assert lib.fd_plan_sms(B, NH, NKV, HS, cap, win, 0, 152, 2, 8, ctypes.byref(p)) == code
     # fd_decode_attn checks the shape before it touches the device
     assert lib.fd_decode_attn(16, 16, 16, 16, 16, B, NH, NKV, HS, cap, win, 0.0, None) == code
 
@@ -149,7 +169,7 @@ def test_pointer_and_workspace_errors_before_any_cuda_call(lib):
     # null plan
     assert ex(None, A, p.workspace_bytes, None, A, A, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
     # B == 0 is a no-op success
-    p0 = fd.fd_plan_sms(0, 16, 8, 256, 64, 0, 0, 152, 2)
+    p0 = fd.fd_plan_sms(0, 16, 8, 256, 64, 0, 0, 152, 2, 8)
     assert ex(ctypes.byref(p0), None, 0, None, None, None, None, None, None,
               0, 16, 8, 256, 64, 0, 0.0, None) == fd.FD_OK
     assert lib.fd_get_device_error(None, None) == fd.FD_ERR_INVALID_ARG

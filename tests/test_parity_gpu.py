@@ -80,11 +80,36 @@ def test_result_independent_of_split_count(w):
     band = max(min(int(x), w.window if w.window > 0 else w.capacity) for x in lens)
     outs = []
     for s in sorted({1, 2, 3, 7, 64, band, band + 5}):
-        res = run(w, q, k, v, lens, splits=s)
+        res = run(w, q, k, v, lens, splits=s, cluster=1)
         check(res, ref, what=f"{w.name} S={s}")
         outs.append(res["out32"])
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() <= 2e-3
+
+
+CLUSTER_CASES = [
+    W("cl_mqa", 2, 16, 1, 512, 700, 0, lens=(700, 3), seed=61),
+    W("cl_ring", 1, 16, 8, 256, 256, 200, lens=(1234,), seed=62),
+    W("cl_llama", 3, 32, 8, 128, 400, 0, lens=(400, 1, 0), seed=63),
+    W("cl_g16_d64", 1, 16, 1, 64, 300, 0, lens=(299,), seed=64),
+]
+
+
+@pytest.mark.parametrize("w", CLUSTER_CASES, ids=[c.name for c in CLUSTER_CASES])
+def test_result_independent_of_cluster_size(w):
+    """Thread-block clusters that combine partials in distributed shared
+    memory, with one cluster per band (direct output) or several (merged
+    partials), agree with the oracle for every cluster size."""
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    maxc = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window).max_cluster
+    for cluster in (1, 2, 4, 8, 16):
+        if cluster > maxc or (w.HS // cluster) % 4:
+            continue
+        for splits in sorted({cluster, 2 * cluster, 3 * cluster, 8 * cluster}):
+            res = run(w, q, k, v, lens, splits=splits, cluster=cluster)
+            check(res, ref, what=f"{w.name} S={splits} cluster={cluster}")
+            assert res["deverr"] == 0
 
 
 def test_single_position_band_returns_v_exactly():
@@ -93,7 +118,7 @@ def test_single_position_band_returns_v_exactly():
         q, k, v, lens = make_inputs(w)
         for path in (fd.FD_PATH_TC, fd.FD_PATH_SIMT):
             for splits in (0, 1, 5):
-                res = run(w, q, k, v, lens, splits=splits, path=path)
+                res = run(w, q, k, v, lens, splits=splits, path=path, cluster=1 if splits else 0)
                 G = w.NH // w.NKV
                 for h in range(w.NH):
                     vrow = v[0, h // G, slot]

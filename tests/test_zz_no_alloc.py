@@ -30,7 +30,8 @@ pytestmark = pytest.mark.gpu
 CASES = [
     Workload("noalloc_ring", 1, 16, 8, 256, 1024, 1024, lens=(5000,), seed=501),
     Workload("noalloc_mqa", 2, 16, 1, 512, 4096, 0, lens=(4096, 1234), seed=502),
-    Workload("noalloc_ragged", 4, 32, 8, 128, 2048, 0, lens=(1, 2048, 700, 33), seed=503),
+    Workload("noalloc_ragged", 16, 32, 8, 128, 2048, 0,
+             lens=(1, 2048, 700, 33, 1500, 2, 999, 2047, 64, 65, 1024, 300, 3, 1800, 512, 17), seed=503),
 ]
 
 
