@@ -48,7 +48,10 @@ class fd_plan_t(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_int),
         ("num_sms", ctypes.c_int),
         ("max_cluster", ctypes.c_int),
+        ("fused", ctypes.c_int),
+        ("group_bytes", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
+        ("workspace_zero_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),
         ("NH", ctypes.c_int),
         ("NKV", ctypes.c_int),
@@ -85,7 +88,7 @@ def load_library(path: Path | str | None = None):
     sig = {
         "fd_plan": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_sms": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
-        "fd_plan_override": (ci, [planp, ci, ci, ci]),
+        "fd_plan_override": (ci, [planp, ci, ci, ci, ci]),
         "fd_workspace_bytes": (sz, [planp]),
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
@@ -151,8 +154,10 @@ def fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm,
     return p
 
 
-def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO, cluster: int = 0) -> fd_plan_t:
-    _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path, cluster), "fd_plan_override")
+def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO, cluster: int = 0,
+                     fused: int = -1) -> fd_plan_t:
+    _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path, cluster, fused),
+           "fd_plan_override")
     return plan
 
 

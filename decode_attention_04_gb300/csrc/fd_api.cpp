@@ -37,14 +37,55 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Partial slots per row: one per block, or one per cluster of blocks.
 int slots(const fd_plan_t& p) { return p.num_splits / (p.cluster > 0 ? p.cluster : 1); }
 
-// Bytes of the (O) part of the workspace; the (m, l) part follows it.
+// Workspace layout when a row has more than one partial slot:
+//   [counters: B*NKV uint32, must be zero before the first call]
+//   [O partials: fp32 B*NH*slots*HS] [(m, l): fp32 B*NH*slots*2]
+// each part rounded up to 256 bytes.
+size_t ws_counter_bytes(const fd_plan_t& p) {
+  if (slots(p) <= 1) return 0;
+  return round_up(static_cast<size_t>(p.B) * p.NKV * sizeof(unsigned int), 256);
+}
+
 size_t ws_o_bytes(const fd_plan_t& p) {
   return round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * p.HS * sizeof(float), 256);
 }
 
 size_t ws_total(const fd_plan_t& p) {
   if (slots(p) <= 1) return 0;
-  return ws_o_bytes(p) + round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * 2 * sizeof(float), 256);
+  return ws_counter_bytes(p) + ws_o_bytes(p) +
+         round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * 2 * sizeof(float), 256);
+}
+
+// Fused merge (the last split block of each (sequence, KV head) merges) when
+// the group's partials are few and small: G * S weights fit the block's score
+// buffer and the partials stay within 256 KB per group.
+bool fused_rule_allowed(const fd_plan_t& p) {
+  const long long G = p.NH / p.NKV;
+  return p.path == FD_PATH_TC && p.cluster == 1 && slots(p) > 1 && G * p.num_splits <= 480;
+}
+
+// Off by default: measured on GB300, the separate merge kernel (already
+// resident through programmatic dependent launch, 128+ blocks pulling the
+// partials in parallel) beat the last block merging alone on every workload
+// here. Kept as an option (fd_plan_override) and tested both ways.
+int fused_rule(const fd_plan_t& p) {
+  (void)p;
+  return 0;
+}
+
+// 4 KB copy groups (a tile that needs the whole SM) only for the head-dim-512,
+// 16-row tile, and only when the grid fits one wave at one block per SM.
+int group_rule(const fd_plan_t& p) {
+  const long long G = p.NH / p.NKV;
+  const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
+  return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
+}
+
+void finish_plan(fd_plan_t* p, int fused = -1) {
+  p->fused = fused < 0 ? fused_rule(*p) : (fused && fused_rule_allowed(*p) ? 1 : 0);
+  p->group_bytes = group_rule(*p);
+  p->workspace_bytes = ws_total(*p);
+  p->workspace_zero_bytes = ws_counter_bytes(*p);
 }
 
 bool valid_cluster(int cluster, int num_splits, int HS, int path) {
@@ -117,7 +158,7 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   p.HS = HS;
   p.capacity = capacity;
   p.window = window;
-  p.workspace_bytes = ws_total(p);
+  finish_plan(&p);
   *plan = p;
   return FD_OK;
 }
@@ -172,6 +213,10 @@ int get_workspace(int device, cudaStream_t stream, size_t need, void** ptr) {
   }
   void* p = nullptr;
   if (cudaMalloc(&p, need) != cudaSuccess) return FD_ERR_CUDA;
+  if (cudaMemset(p, 0, need) != cudaSuccess) {  // the counters must start at zero
+    cudaFree(p);
+    return FD_ERR_CUDA;
+  }
   w.ptr = p;
   w.bytes = need;
   *ptr = p;
@@ -200,8 +245,12 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.out = static_cast<uint16_t*>(out);
   a.out_f32 = out_f32;
   a.lens = lens;
-  a.ws_o = need ? static_cast<float*>(workspace) : nullptr;
-  a.ws_ml = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws_o_bytes(plan)) : nullptr;
+  char* ws = static_cast<char*>(workspace);
+  a.counters = need ? reinterpret_cast<unsigned int*>(ws) : nullptr;
+  a.ws_o = need ? reinterpret_cast<float*>(ws + ws_counter_bytes(plan)) : nullptr;
+  a.ws_ml = need ? reinterpret_cast<float*>(ws + ws_counter_bytes(plan) + ws_o_bytes(plan)) : nullptr;
+  a.fused = plan.fused;
+  a.group_bytes = plan.group_bytes;
   a.B = plan.B;
   a.NH = plan.NH;
   a.NKV = plan.NKV;
@@ -245,7 +294,7 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
   return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, max_cluster, FD_PATH_AUTO, plan);
 }
 
-int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster) {
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int fused) {
   if (!plan || num_splits < 0 || cluster < 0 || num_splits > 65535 * 64) return FD_ERR_INVALID_ARG;
   if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_TC) return FD_ERR_INVALID_ARG;
   if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
@@ -259,7 +308,8 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster) {
   if (cluster > 0) p.cluster = cluster;
   if (p.path == FD_PATH_SIMT && cluster == 0) p.cluster = 1;  // the SIMT path has no clusters
   if (!valid_cluster(p.cluster, p.num_splits, p.HS, p.path)) return FD_ERR_INVALID_ARG;
-  p.workspace_bytes = ws_total(p);
+  if (fused > 0 && !fused_rule_allowed(p)) return FD_ERR_INVALID_ARG;
+  finish_plan(&p, fused);
   *plan = p;
   return FD_OK;
 }
@@ -277,7 +327,10 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
       plan->window != window)
     return FD_ERR_INVALID_ARG;
   if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1 ||
-      !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path))
+      !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
+      (plan->fused && !fused_rule_allowed(*plan)) || (plan->group_bytes != 2048 && plan->group_bytes != 4096) ||
+      (plan->group_bytes == 4096 && group_rule(*plan) != 4096 &&
+       !(plan->HS == 512 && plan->NH / plan->NKV > 8 && plan->path == FD_PATH_TC)))
     return FD_ERR_INVALID_ARG;
   return run(*plan, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens, scale,
              reinterpret_cast<cudaStream_t>(stream));

@@ -20,6 +20,9 @@ struct LaunchArgs {
   const int* lens;          // int32 [B]
   float* ws_o;              // fp32 [B][NH][S][HS]  (S > 1 only)
   float* ws_ml;             // fp32 [B][NH][S][2]   (m in log2 units, l)
+  unsigned int* counters;   // [B][NKV] finished-split counters (fused merge), zero between calls
+  int fused;                // 1: the last split block of each (b, kvh) merges; no merge kernel
+  int group_bytes;          // bytes per bulk-copy group of the tile (2048, or 4096 for the wide MQA tile)
   int B, NH, NKV, HS, capacity, window;  // window <= 0: none
   int num_splits;           // S
   int cluster;              // blocks per cluster along the splits (S % cluster == 0)

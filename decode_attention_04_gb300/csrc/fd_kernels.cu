@@ -341,10 +341,10 @@ size_t simt_smem_bytes(int G, int HS) {
 // ===================================================== tensor-core split kernel
 
 // Shared-memory staging of a tile. The K (and V) rows of a tile arrive as NG
-// groups of R consecutive positions, 2 KB per group, so one bulk copy moves a
-// whole group: a block's copy rate is set by the number of copies it issues
-// (on GB300, about 15 / 23 / 33 GB/s per block with 0.5 / 1 / 2 KB copies),
-// not by their bytes. Groups are 16 bytes apart beyond their R rows. Row i of
+// groups of R consecutive positions, GROUP_BYTES (2 or 4 KB) per group, so one
+// bulk copy moves a whole group: a block's copy rate is set by the number of
+// copies it issues (on GB300, about 15 / 23 / 33 / 45 GB/s per block with
+// 0.5 / 1 / 2 / 4 KB copies), not by their bytes. Groups are 16 bytes apart beyond their R rows. Row i of
 // group g holds tile position g*R + i.
 //
 // The MMAs walk the tile in a permuted order: MMA row m takes group m % NG,
@@ -352,7 +352,7 @@ size_t simt_smem_bytes(int G, int HS) {
 // i.e. in eight different 16-byte bank groups, so every 8-row ldmatrix is
 // conflict-free. Scores, P and the P.V contraction all use the same order;
 // the softmax does not depend on the order of positions.
-template <int HS_, int NT_, int NWC_, int NSTAGE_>
+template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048>
 struct TcCfg {
   static constexpr int HS = HS_;
   static constexpr int NT = NT_;          // 8-row tiles of query rows (G <= 8 * NT)
@@ -360,7 +360,7 @@ struct TcCfg {
   static constexpr int NWC = NWC_;        // consumer warps
   static constexpr int NSTAGE = NSTAGE_;  // shared-memory ring depth
   static constexpr int ROWB = HS * 2;     // bytes of one cache row
-  static constexpr int R = ROWB >= 2048 ? 1 : 2048 / ROWB;  // rows per group
+  static constexpr int R = ROWB >= GROUP_BYTES_ ? 1 : GROUP_BYTES_ / ROWB;  // rows per group
   static constexpr int NG = 8;            // groups per tile
   static constexpr int T = NG * R;        // positions per pipeline tile
   static constexpr int GP = R * ROWB + 16;  // group pitch, bytes
@@ -398,6 +398,7 @@ struct TcCfg {
   // cluster reduction: O parked in the K stages, weights in the score buffer
   static_assert(static_cast<size_t>(NP) * HS * 4 <= NSTAGE * STAGE_BYTES, "O must fit the K stages");
   static_assert(NP * 16 + 2 * NP <= NWC * T * NP, "cluster weights must fit the score buffer");
+  static_assert(NWC * T * NP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
 
 template <class C>
@@ -445,7 +446,9 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int n = p0 < p1 ? static_cast<int>(p1 - p0) : 0;
 
   if (n == 0 && CS == 1) {
-    if (direct) {  // len == 0: the output row is zero
+    // len == 0: the output row is zero. With one block per band, or with the
+    // fused merge (no block of an empty band ever merges), block 0 writes it.
+    if (direct || (a.fused && band == 0 && s == 0)) {
       for (int i = tid; i < G * C::HS; i += C::THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / C::HS) * C::HS + i % C::HS;
         a.out[o] = 0;
@@ -704,6 +707,74 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       a.ws_ml[r] = sM[tid];
       a.ws_ml[r + 1] = sL[tid];
     }
+    if (direct || !a.fused) return;
+
+    // ---- fused merge: the last block of this (sequence, KV head) to finish
+    // combines every partial of the group (no merge launch). The counter
+    // wraps to zero as the last block takes it, so it is zero again for the
+    // next call.
+    __shared__ int s_last;
+    const int nsplit = active_splits(band, chunk);
+    named_bar_sync(1, C::CTHREADS);  // every thread's partial stores precede ...
+    if (tid == 0) {
+      __threadfence();  // ... this fence (cumulative), so they are visible before the count
+      s_last = atomicInc(a.counters + static_cast<size_t>(b) * a.NKV + kvh, static_cast<unsigned>(nsplit - 1)) ==
+               static_cast<unsigned>(nsplit - 1);
+      __threadfence();  // and every counted partial is visible after it
+    }
+    named_bar_sync(1, C::CTHREADS);
+    if (!s_last) return;
+
+    const int S = a.num_splits;
+    float* sW = sS;            // [G][nsplit] weights 2^(m_s - M)
+    float* sLt = sAlpha;       // [G] sum of weighted l
+    for (int g = warp; g < G; g += C::NWC) {
+      const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + (static_cast<size_t>(b) * a.NH + hbase + g) * S;
+      float M = kNegInf;
+      for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, __ldcg(&ml[j].x));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      float L = 0.f;
+      for (int j = lane; j < nsplit; j += 32) {
+        const float2 v = __ldcg(&ml[j]);
+        const float w = exp2f(v.x - M);
+        sW[g * nsplit + j] = w;
+        L += w * v.y;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      if (lane == 0) sLt[g] = L;
+    }
+    named_bar_sync(1, C::CTHREADS);
+    constexpr int D4 = C::HS / 4;
+    for (int it = tid; it < G * D4; it += C::CTHREADS) {
+      const int g = it / D4, d = (it % D4) * 4;
+      const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
+      const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * S * C::HS + d);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < nsplit; j0 += 8) {  // 8 loads in flight per thread
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = j0 + u < nsplit ? __ldcg(src + static_cast<size_t>(j0 + u) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = j0 + u < nsplit ? sW[g * nsplit + j0 + u] : 0.f;
+          acc.x += w * v[u].x;
+          acc.y += w * v[u].y;
+          acc.z += w * v[u].z;
+          acc.w += w * v[u].w;
+        }
+      }
+      const float L = sLt[g];
+      const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+      const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+      const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+      *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+    }
     return;
   }
 
@@ -920,7 +991,9 @@ cudaError_t occupancy_tc(int* ctas) {
 }
 
 // Tile configurations: 8 groups of 2 KB per tensor per stage (about 33 KB of
-// K+V), three stages; G <= 8 or G <= 16 query rows per group.
+// K+V), three stages, two blocks per SM; G <= 8 or G <= 16 query rows per
+// group. The head-dim-512, 16-row tile (the MQA geometry, planned with one
+// block per SM) uses 4 KB groups: 66 KB stages, ~204 KB of shared memory.
 using Tc64x1 = TcCfg<64, 1, 4, 3>;
 using Tc64x2 = TcCfg<64, 2, 4, 3>;
 using Tc128x1 = TcCfg<128, 1, 4, 3>;
@@ -929,15 +1002,18 @@ using Tc256x1 = TcCfg<256, 1, 4, 3>;
 using Tc256x2 = TcCfg<256, 2, 4, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;
 using Tc512x2 = TcCfg<512, 2, 4, 3>;
+using Tc512x2w = TcCfg<512, 2, 4, 3, 4096>;  // one block per SM, 4 KB copies
 
 template <template <class> class Fn, class... Args>
-cudaError_t with_tc_cfg(int HS, int G, Args&&... args) {
+cudaError_t with_tc_cfg(int HS, int G, int group_bytes, Args&&... args) {
   const bool two = G > 8;
   switch (HS) {
     case 64: return two ? Fn<Tc64x2>::run(args...) : Fn<Tc64x1>::run(args...);
     case 128: return two ? Fn<Tc128x2>::run(args...) : Fn<Tc128x1>::run(args...);
     case 256: return two ? Fn<Tc256x2>::run(args...) : Fn<Tc256x1>::run(args...);
-    case 512: return two ? Fn<Tc512x2>::run(args...) : Fn<Tc512x1>::run(args...);
+    case 512:
+      if (!two) return Fn<Tc512x1>::run(args...);
+      return group_bytes >= 4096 ? Fn<Tc512x2w>::run(args...) : Fn<Tc512x2>::run(args...);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1015,10 +1091,12 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas) {
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_simt_kernel, kSimtThreads, sm);
   }
-  return with_tc_cfg<OccFn>(HS, G, ctas);
+  return with_tc_cfg<OccFn>(HS, G, 2048, ctas);
 }
 
-cudaError_t query_max_cluster(int HS, int G, int* cluster) { return with_tc_cfg<MaxClusterFn>(HS, G, cluster); }
+cudaError_t query_max_cluster(int HS, int G, int* cluster) {
+  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, cluster);
+}
 
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
   const int G = a.NH / a.NKV;
@@ -1030,9 +1108,11 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     dim3 grid(a.num_splits, a.NKV, a.B);
     e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, 1, a);
   } else {
-    e = with_tc_cfg<LaunchFn>(a.HS, G, a, stream);
+    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a, stream);
   }
-  if (e != cudaSuccess || a.num_splits == a.cluster) return e;  // the split kernel wrote the output
+  // the split kernel wrote the output itself: one block / cluster per band, or
+  // the fused merge by each group's last block
+  if (e != cudaSuccess || a.num_splits == a.cluster || a.fused) return e;
   dim3 mgrid(a.HS / 32, a.NH, a.B);
   return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
 }

@@ -17,12 +17,17 @@
 // never handed to a kernel: the device address comes from
 // cudaGetSymbolAddress, taken once per device with that device current.
 //
-// Nothing in the scratch has to start at zero: every partial the merge kernel
-// reads is written earlier in the same call, so no clearing is needed between
-// calls even though each call finds the previous call's contents there. All
-// calls on a device share the one array, so calls that overlap on the GPU (on
-// different streams, or from different threads) race on it and must be
-// serialised by the caller.
+// The scratch starts with a fixed 64 KB region that holds only split counters
+// (one per (sequence, KV head), up to 16384 of them), then the partials. Each
+// call hands fd_decode_attn_ex a workspace that begins inside that region so
+// that its counters end exactly where the region ends: partials of one shape
+// can then never land on another shape's counters. The set-up of a device
+// clears the whole array once; every completed call leaves its counters at
+// zero again, and every partial a call reads was written earlier in the same
+// call, so nothing is cleared between calls although each call finds the
+// previous call's contents there. All calls on a device share the
+// one array, so calls that overlap on the GPU (on different streams, or from
+// different threads) race on it and must be serialised by the caller.
 
 #include <map>
 #include <mutex>
@@ -35,13 +40,15 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[FD_NOALLOC_SCRATCH_BYTES];
 
+constexpr size_t kCounterRegion = 64u << 10;  // split counters of up to 16384 groups
+
 std::mutex g_scratch_mu;
 std::map<int, void*> g_scratch_addr;  // device -> device address of the array
 
 // Device address of the scratch array on `device`, which must be the current
 // device. The first call for a device performs the lookup (and, with lazy
-// module loading, loads this module on that device); later calls return the
-// cached address.
+// module loading, loads this module on that device) and clears the array;
+// later calls return the cached address.
 int scratch_address(int device, void** ptr) {
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   auto it = g_scratch_addr.find(device);
@@ -51,6 +58,9 @@ int scratch_address(int device, void** ptr) {
   }
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FD_ERR_CUDA;
+  // The split counters at the head of the scratch must start at zero (every
+  // completed call leaves them zero again); clear the whole array once.
+  if (cudaMemset(p, 0, FD_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return FD_ERR_CUDA;
   g_scratch_addr[device] = p;
   *ptr = p;
   return FD_OK;
@@ -71,12 +81,17 @@ extern "C" int fd_decode_attn_noalloc(const void* q, const void* k_cache, const 
   if (cudaGetDevice(&device) != cudaSuccess) return FD_ERR_CUDA;
   rc = fd_plan(B, NH, NKV, HS, capacity, window, 0, device, &plan);
   if (rc != FD_OK) return rc;
-  if (plan.workspace_bytes > FD_NOALLOC_SCRATCH_BYTES) return FD_ERR_SCRATCH_LIMIT;
+  const size_t counters = plan.workspace_zero_bytes;
+  if (counters > kCounterRegion ||
+      plan.workspace_bytes - counters > FD_NOALLOC_SCRATCH_BYTES - kCounterRegion)
+    return FD_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   if (plan.workspace_bytes > 0) {
-    rc = scratch_address(device, &ws);
+    void* base = nullptr;
+    rc = scratch_address(device, &base);
     if (rc != FD_OK) return rc;
+    ws = static_cast<unsigned char*>(base) + (kCounterRegion - counters);
   }
-  return fd_decode_attn_ex(&plan, ws, FD_NOALLOC_SCRATCH_BYTES, nullptr, q, k_cache, v_cache, out, lens, B, NH,
-                           NKV, HS, capacity, window, scale, stream);
+  return fd_decode_attn_ex(&plan, ws, plan.workspace_bytes, nullptr, q, k_cache, v_cache, out, lens, B, NH, NKV,
+                           HS, capacity, window, scale, stream);
 }

@@ -105,6 +105,17 @@ enum {
  * next to a split's K/V bytes, and the plan fills each SM once instead of
  * with every resident block.
  *
+ * Fused merge (opt-in through fd_plan_override; plans use fused = 0): when a
+ * group has few partials (G * S <= 480), the last split block of each
+ * (sequence, KV head) to finish merges them itself, found with a per-group
+ * counter that wraps back to zero; no merge kernel is launched.
+ *
+ * Copy groups: a tile's K and V rows arrive in groups of about 2 KB, one
+ * bulk copy per group. For head dim 512 with more than 8 query rows per KV
+ * head, when the whole grid fits one wave at one block per SM, the plan uses
+ * 4 KB groups (a tile that needs the whole SM's shared memory): fewer copies
+ * per block, and a block's copy rate is set by its copy count.
+ *
  * Clusters (opt-in through fd_plan_override; plans use cluster = 1): the
  * blocks of `cluster` consecutive splits form a thread-block cluster and
  * combine their partials through distributed shared memory, so only
@@ -121,7 +132,10 @@ typedef struct {
   int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
   int num_sms;             /* SM count the plan assumed */
   int max_cluster;         /* largest cluster the device schedules for this kernel */
+  int fused;               /* 1: each group's last split block merges (no merge kernel) */
+  int group_bytes;         /* bytes per bulk-copy group of a tile: 2048, or 4096 (see below) */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
+  size_t workspace_zero_bytes; /* leading workspace bytes that must be zero before first use */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
   int B, NH, NKV, HS, capacity, window;
 } fd_plan_t;
@@ -147,19 +161,24 @@ int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int ma
 
 /*
  * fd_plan_override: force the split count (num_splits >= 1; 0 keeps the
- * plan's), the kernel family (path != FD_PATH_AUTO) and/or the cluster size
+ * plan's), the kernel family (path != FD_PATH_AUTO), the cluster size
  * (cluster >= 1, a power of two <= 16 that divides num_splits and HS / 4;
- * 0 keeps the plan's; the SIMT path takes cluster 1 only), recomputing
- * workspace_bytes. Used to test that the result does not depend on the split
- * count or the cluster size, and to bisect. Errors: FD_ERR_INVALID_ARG.
+ * 0 keeps the plan's; the SIMT path takes cluster 1 only) and/or the fused
+ * merge (fused = 0 off, 1 on where allowed, -1 the plan's rule), then
+ * recompute the dependent fields (fused, group_bytes, workspace sizes). Used
+ * to test that the result does not depend on these choices, and to bisect.
+ * Errors: FD_ERR_INVALID_ARG.
  */
-int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster);
+int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int fused);
 
 /*
- * fd_workspace_bytes: workspace the partials of a plan need: with
- * P = num_splits / cluster partial slots per row, B * NH * P * (HS + 2) * 4
- * bytes, each part rounded up to 256 (0 when P == 1: the split kernel then
- * writes the output itself).
+ * fd_workspace_bytes: workspace a plan needs. With P = num_splits / cluster
+ * partial slots per row and P > 1: B * NKV 32-bit split counters, then
+ * B * NH * P * HS fp32 partial outputs, then B * NH * P * 2 fp32 (m, l), each
+ * part rounded up to 256 bytes. 0 when P == 1 (the split kernel then writes
+ * the output itself). The counters (the first workspace_zero_bytes bytes)
+ * must be zero before a workspace's first use; every completed call leaves
+ * them zero.
  */
 size_t fd_workspace_bytes(const fd_plan_t* plan);
 
@@ -180,10 +199,12 @@ int fd_decode_attn(const void* q, const void* k_cache, const void* v_cache, void
 
 /*
  * fd_decode_attn_ex: the same with an explicit plan, a caller-owned device
- * workspace of workspace_bytes >= fd_workspace_bytes(plan) (contents need no
- * initialisation and are scratch between calls; calls that overlap on the GPU
- * must not share one), and an optional fp32 copy of the output (out_f32 may be
- * NULL). The shape arguments must equal the plan's. Allocates nothing.
+ * workspace of workspace_bytes >= fd_workspace_bytes(plan) whose first
+ * plan->workspace_zero_bytes bytes were zero before its first use (every
+ * completed call leaves them zero; the rest is scratch between calls; calls
+ * that overlap on the GPU must not share one), and an optional fp32 copy of
+ * the output (out_f32 may be NULL). The shape arguments must equal the plan's.
+ * Allocates nothing.
  * Errors: every FD_ERR_* code.
  */
 int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes,
@@ -203,16 +224,19 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
  * counterpart on the pages; it is an addition of this library.
  *   - Same arguments, layouts and conventions as fd_decode_attn; the plan is
  *     made for the current device with max_len <= 0.
- *   - A shape whose plan needs more than FD_NOALLOC_SCRATCH_BYTES of
- *     workspace is rejected with FD_ERR_SCRATCH_LIMIT before anything is
- *     launched (fd_plan + fd_workspace_bytes tell in advance).
+ *   - The array holds split counters for up to 16384 (sequence, KV head)
+ *     pairs in its first 64 KB and partials in the rest. A shape whose plan
+ *     needs more (B * NKV > 16384, or more than 32 MiB - 64 KB of partials)
+ *     is rejected with FD_ERR_SCRATCH_LIMIT before anything is launched
+ *     (fd_plan + fd_workspace_bytes tell in advance).
  *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress) and caches it; make that first call before
- *     any stream capture.
+ *     device (cudaGetSymbolAddress), clears the array (cudaMemset) and caches
+ *     the address; make that first call before any stream capture.
  *   - All calls on a device share the one array and each finds the previous
- *     call's contents in it (nothing there needs to start at zero). Calls that
- *     overlap on the GPU - other streams, other threads - race on it: the
- *     caller must serialise them.
+ *     call's contents in it. The counters must start at zero: the device's
+ *     set-up clears the array once and every completed call leaves them zero.
+ *     Calls that overlap on the GPU - other streams, other threads - race on
+ *     it: the caller must serialise them.
  * Errors: every FD_ERR_* code.
  */
 int fd_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out,

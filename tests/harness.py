@@ -43,7 +43,8 @@ class Guarded:
 
 
 def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len: int = 0,
-        poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None, cluster: int = 0):
+        poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None, cluster: int = 0,
+        fused: int = -1):
     """One fd_decode_attn_ex call. Returns dict with out (bf16, cpu), out32
     (fp32, cpu), plan, deverr, canaries (bool)."""
     dev = torch.device(device)
@@ -52,21 +53,24 @@ def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len:
     else:
         qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len)
-    if splits or path or cluster:
-        fd.fd_plan_override(plan, splits, path, cluster)
+    if splits or path or cluster or fused >= 0:
+        fd.fd_plan_override(plan, splits, path, cluster, fused)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)         # NaN-filled: unwritten rows show up
     o32 = Guarded(n * 4, dev, fill=0xFF)
     ws = Guarded(plan.workspace_bytes, dev, fill=0xFF if poison_ws else 0)
+    if plan.workspace_zero_bytes:  # the split counters must start at zero
+        ws.body[: plan.workspace_zero_bytes].zero_()
     fd.fd_get_device_error()  # clear
     fd.fd_decode_attn_ex(plan, ws.ptr() if plan.workspace_bytes else None, plan.workspace_bytes, o32.ptr(),
                          qd, kd, vd, o16.ptr(), ld, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
                          w.scale if scale is None else scale)
     torch.cuda.synchronize()
     err = fd.fd_get_device_error()
+    counters_zero = bool((ws.body[: plan.workspace_zero_bytes] == 0).all().item()) if plan.workspace_zero_bytes else True
     return dict(out=o16.view(torch.bfloat16, (w.B, w.NH, w.HS)).cpu(),
                 out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(),
-                plan=plan, deverr=err,
+                plan=plan, deverr=err, counters_zero=counters_zero,
                 canaries=o16.canaries_intact() and o32.canaries_intact() and ws.canaries_intact())
 
 
@@ -81,6 +85,7 @@ def check(res: dict, ref: np.ndarray, rows=None, what: str = ""):
     """Assert the GPU result matches the oracle within the tolerances, on all
     rows or on the (b, h) pairs in `rows`."""
     assert res["canaries"], f"{what}: guard canary overwritten"
+    assert res["counters_zero"], f"{what}: split counters not back to zero after the call"
     out32 = res["out32"].double().numpy()
     out16 = res["out"].view(torch.int16).numpy().view(np.uint16)
     if rows is not None:

@@ -71,8 +71,16 @@ def test_plan_fills_the_gpu_and_sizes_workspace(name, lib):
     assert units * active >= 0.9 * min(152 * per_sm, units * -(-band // p.granule))
     P = p.num_splits // p.cluster
     assert p.num_splits % p.cluster == 0
-    expect_ws = 0 if P == 1 else (
-        -(-(w.B * w.NH * P * w.HS * 4) // 256) * 256 + -(-(w.B * w.NH * P * 8) // 256) * 256)
+    up = lambda x: -(-x // 256) * 256
+    expect_zero = 0 if P == 1 else up(w.B * w.NKV * 4)
+    expect_ws = 0 if P == 1 else expect_zero + up(w.B * w.NH * P * w.HS * 4) + up(w.B * w.NH * P * 8)
+    assert p.workspace_zero_bytes == expect_zero
+    assert p.fused == 0  # the fused merge is opt-in
+    G = w.NH // w.NKV
+    if P > 1 and G * p.num_splits <= 480:
+        q = fd.fd_plan_t.from_buffer_copy(p)
+        fd.fd_plan_override(q, 0, 0, 0, 1)
+        assert q.fused == 1 and q.workspace_bytes == p.workspace_bytes
     assert p.workspace_bytes == expect_ws == fd.fd_workspace_bytes(p)
     # workspace is bounded by partials, never by the cache allocation
     assert p.workspace_bytes <= 32 << 20

@@ -87,6 +87,32 @@ def test_result_independent_of_split_count(w):
         assert (o - outs[0]).abs().max().item() <= 2e-3
 
 
+FUSED_CASES = [
+    W("fu_ring", 1, 16, 8, 256, 1024, 1024, lens=(32768,), seed=71),
+    W("fu_llama_batch", 5, 32, 8, 128, 600, 0, lens=(600, 0, 1, 299, 64), seed=72),
+    W("fu_g8_d512", 2, 16, 2, 512, 300, 0, lens=(300, 17), seed=73),
+]
+
+
+@pytest.mark.parametrize("w", FUSED_CASES, ids=[c.name for c in FUSED_CASES])
+def test_fused_merge_equals_merge_kernel(w):
+    """The last split block of each group merging the partials itself (no merge
+    kernel) agrees with the oracle and with the separate merge kernel, for split
+    counts from 2 up to the fused limit; the counters are back at zero after
+    every call."""
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    G = w.NH // w.NKV
+    for S in sorted({2, 3, 8, 19, 38, 480 // G}):
+        outs = {}
+        for fused in (0, 1):
+            res = run(w, q, k, v, lens, splits=S, cluster=1, fused=fused)
+            assert res["plan"].fused == fused
+            check(res, ref, what=f"{w.name} S={S} fused={fused}")
+            outs[fused] = res["out32"]
+        assert (outs[0] - outs[1]).abs().max().item() <= 1e-5
+
+
 CLUSTER_CASES = [
     W("cl_mqa", 2, 16, 1, 512, 700, 0, lens=(700, 3), seed=61),
     W("cl_ring", 1, 16, 8, 256, 256, 200, lens=(1234,), seed=62),
@@ -145,7 +171,7 @@ def test_repeat_runs_are_bitwise_identical():
     dev = torch.device("cuda")
     qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
-    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     first = None
     for _ in range(100):
         out = torch.empty_like(qd)

@@ -43,7 +43,7 @@ def _on_device(w, seed):
 
 def _explicit(w, q, k, v, lens):
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
-    ws = torch.empty(max(1, plan.workspace_bytes), dtype=torch.uint8, device=q.device)
+    ws = torch.zeros(max(1, plan.workspace_bytes), dtype=torch.uint8, device=q.device)
     out = torch.empty_like(q)
     fd.fd_decode_attn_ex(plan, ws, plan.workspace_bytes, None, q, k, v, out, lens, w.B, w.NH, w.NKV, w.HS,
                          w.capacity, w.window, w.scale)
