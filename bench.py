@@ -54,6 +54,28 @@ def live_band_bytes(w, lens) -> int:
     return tot * w.NKV * w.HS * 2 * 2
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Largest value of x over the ranks of the default process group (x
+    itself without one): a replica job is as slow as its slowest rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(bytes_per_step_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job live-band GB/s: every rank's bytes over the slowest step."""
+    return bytes_per_step_per_rank * world / (ms_per_step * 1e-3) / 1e9
+
+
+def kernels_per_call(plan) -> int:
+    """Kernels one call launches: the split kernel, plus the merge kernel
+    unless one block/cluster spans every split or the fused merge is on."""
+    return 1 if (plan.num_splits == plan.cluster or plan.fused) else 2
+
+
 def measured_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -302,7 +324,7 @@ def main():
     step = Step(w, layers_for(w, 0), device)
     L = step.L
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
-    kernels_per_call = 1 if plan.num_splits == 1 else 2
+    launches_per_call = kernels_per_call(plan)
 
     # ---- device-timed steps (graph replay), clocks sampled during the region
     if world > 1:
@@ -312,21 +334,19 @@ def main():
     with ClockSampler(local) as clk:
         ms, graph = time_graph(step, args.steps, args.warmup, stream)
     torch.cuda.synchronize()
-    tot_ms = sum(ms)
+    tot_ms = max_over_ranks(sum(ms), device)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([tot_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-        tot_ms = t.item()
     ms_per_step = tot_ms / args.steps
-    value = step.live * L * world / (ms_per_step * 1e-3) / 1e9
+    value = job_gbps(step.live * L, world, ms_per_step)
     per_layer_us = ms_per_step * 1e3 / L
     achieved = step.live / (per_layer_us * 1e-6) / 1e9
 
     # ---- end to end through the public call, host buffers
     e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
-    e2e_value = step.live * L * world / (statistics.mean(e2e_ms) * 1e-3) / 1e9
+    e2e_ms_per_step = max_over_ranks(statistics.mean(e2e_ms), device)
+    e2e_value = job_gbps(step.live * L, world, e2e_ms_per_step)
 
     if rank != 0:
         if world > 1:
@@ -390,8 +410,8 @@ def main():
             "traffic": traffic,
         },
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": args.steps * L * kernels_per_call,
+                "ms_per_step": e2e_ms_per_step},
+        "gpu_launches": args.steps * L * launches_per_call,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "geometries": geoms,
