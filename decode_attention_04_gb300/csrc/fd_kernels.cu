@@ -364,7 +364,7 @@ struct TcCfg {
   static constexpr int NG = 8;            // groups per tile
   static constexpr int T = NG * R;        // positions per pipeline tile
   static constexpr int GP = R * ROWB + 16;  // group pitch, bytes
-  static constexpr int THREADS = (NWC + 1) * 32;
+  static constexpr int THREADS = (NWC + 2) * 32;  // consumers + a K and a V producer warp
   static constexpr int CTHREADS = NWC * 32;
   static constexpr int DW = HS / NWC;     // head dims owned by one consumer warp
   static constexpr int KD = DW / 16;      // 16-dim steps per warp
@@ -375,8 +375,9 @@ struct TcCfg {
   static constexpr size_t STAGE_BYTES = static_cast<size_t>(NG) * GP;
   static constexpr size_t OFF_K = 0;
   static constexpr size_t OFF_V = OFF_K + NSTAGE * STAGE_BYTES;
-  static constexpr size_t OFF_S = OFF_V + NSTAGE * STAGE_BYTES;              // f32 [NWC][T][NP]
-  static constexpr size_t OFF_P = OFF_S + static_cast<size_t>(NWC) * T * NP * 4;  // bf16 [2][NP][PPITCH]
+  static constexpr int SP = T + 4;       // score row pitch (floats): conflict-free stores and loads
+  static constexpr size_t OFF_S = OFF_V + NSTAGE * STAGE_BYTES;              // f32 [NWC][NP][SP]
+  static constexpr size_t OFF_P = OFF_S + static_cast<size_t>(NWC) * NP * SP * 4;  // bf16 [2][NP][PPITCH]
   static constexpr size_t OFF_A = OFF_P + static_cast<size_t>(2) * NP * PPITCH * 2;  // f32 alpha,m,l [NP]
   static constexpr size_t OFF_BAR = (OFF_A + 3 * NP * 4 + 7) / 8 * 8;        // u64 full[], empty[]
   static constexpr size_t SMEM = OFF_BAR + 2 * NSTAGE * 8;
@@ -397,8 +398,8 @@ struct TcCfg {
   static_assert(NG <= 32, "one producer lane per group");
   // cluster reduction: O parked in the K stages, weights in the score buffer
   static_assert(static_cast<size_t>(NP) * HS * 4 <= NSTAGE * STAGE_BYTES, "O must fit the K stages");
-  static_assert(NP * 16 + 2 * NP <= NWC * T * NP, "cluster weights must fit the score buffer");
-  static_assert(NWC * T * NP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
+  static_assert(NP * 16 + 2 * NP <= NWC * NP * SP, "cluster weights must fit the score buffer");
+  static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
 
 template <class C>
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   // Set-up that reads no input, overlapping the previous kernel's tail.
   if (tid == 0) {
     for (int i = 0; i < C::NSTAGE; ++i) {
-      mbar_init(full0 + 8 * i, 32);         // every producer lane arrives once per phase
+      mbar_init(full0 + 8 * i, 64);         // every lane of both producer warps arrives once per phase
       mbar_init(empty0 + 8 * i, C::NWC);    // one arrival per consumer warp
     }
     fence_mbar_init();
@@ -474,37 +475,37 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   // softmax role: row sr, MMA rows sj + TPR * t
   const int sr = tid / C::TPR, sj = tid % C::TPR;
 
-  if (warp == C::NWC) {
-    // ------------------------------------------------------------ producer
+  if (warp >= C::NWC) {
+    // ----------------------------------------------------------- producers
+    // Warp NWC streams K, warp NWC + 1 streams V: two issuing warps raise a
+    // block's copy rate (a block's rate is set by the copies it issues).
+    const bool is_k = warp == C::NWC;
     const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
-    const uint16_t* kb = a.k + head_row0 * C::HS;
-    const uint16_t* vb = a.v + head_row0 * C::HS;
+    const uint16_t* src = (is_k ? a.k : a.v) + head_row0 * C::HS;
     bool failed = false;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::NSTAGE;
       if (i >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((i / C::NSTAGE) - 1) & 1, failed);
       const int nv = min(C::T, n - i * C::T);
       const long long pbase = p0 + static_cast<long long>(i) * C::T;
-      const uint32_t dk = smem_u32(smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES);
-      const uint32_t dv = smem_u32(smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES);
+      const uint32_t dst =
+          smem_u32(smem + (is_k ? C::OFF_K : C::OFF_V) + static_cast<size_t>(st) * C::STAGE_BYTES);
       const uint32_t fb = full0 + 8 * st;
       // lane g copies group g: rows [g*R, g*R + rows) of the tile
       const int g = lane;
       const int j0 = g * C::R;
       const int rows = (g < C::NG && j0 < nv) ? min(C::R, nv - j0) : 0;
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * 2u * C::ROWB);
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * C::ROWB);
       if (rows > 0) {
         const long long pos0 = pbase + j0;
         const size_t slot0 = static_cast<size_t>(pos0 % a.capacity);
         const uint32_t goff = static_cast<uint32_t>(g) * C::GP;
         if (rows == C::R && slot0 + C::R <= static_cast<size_t>(a.capacity)) {
-          bulk_g2s(dk + goff, kb + slot0 * C::HS, C::R * C::ROWB, fb);
-          bulk_g2s(dv + goff, vb + slot0 * C::HS, C::R * C::ROWB, fb);
+          bulk_g2s(dst + goff, src + slot0 * C::HS, C::R * C::ROWB, fb);
         } else {  // a partial group, or one that wraps around the ring: row by row
           for (int r = 0; r < rows; ++r) {
             const size_t slot = static_cast<size_t>((pos0 + r) % a.capacity);
-            bulk_g2s(dk + goff + r * C::ROWB, kb + slot * C::HS, C::ROWB, fb);
-            bulk_g2s(dv + goff + r * C::ROWB, vb + slot * C::HS, C::ROWB, fb);
+            bulk_g2s(dst + goff + r * C::ROWB, src + slot * C::HS, C::ROWB, fb);
           }
         }
       }
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
 
     // ---- scores: S^T[m][row] partial over this warp's dims (m = MMA row order)
-    float* myS = sS + static_cast<size_t>(warp) * C::T * C::NP;
+    float* myS = sS + static_cast<size_t>(warp) * C::NP * C::SP;
 #pragma unroll
     for (int mt = 0; mt < C::MP; ++mt) {
       if (C::min_pos(mt) < nv) {
@@ -565,9 +566,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         }
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
-          float* d0 = myS + (mt * 16 + grp) * C::NP + nt * 8 + 2 * t4;
-          *reinterpret_cast<float2*>(d0) = make_float2(acc[nt][0], acc[nt][1]);
-          *reinterpret_cast<float2*>(d0 + 8 * C::NP) = make_float2(acc[nt][2], acc[nt][3]);
+          float* d0 = myS + (nt * 8 + 2 * t4) * C::SP + mt * 16 + grp;  // [row][MMA row]
+          d0[0] = acc[nt][0];
+          d0[C::SP] = acc[nt][1];
+          d0[8] = acc[nt][2];
+          d0[C::SP + 8] = acc[nt][3];
         }
       }
     }
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         if (C::pos_of(j) < nv) {
           float acc = 0.f;
 #pragma unroll
-          for (int w = 0; w < C::NWC; ++w) acc += sS[(static_cast<size_t>(w) * C::T + j) * C::NP + sr];
+          for (int w = 0; w < C::NWC; ++w) acc += sS[(static_cast<size_t>(w) * C::NP + sr) * C::SP + j];
           x = acc * a.scale_log2;
         }
         sv[t] = x;
@@ -683,7 +686,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   if (CS == 1) {
     // ---- one block per slice: its partial (O, m, l), or with one split the
     // normalised row
-    if (warp == C::NWC) return;
+    if (warp >= C::NWC) return;
 #pragma unroll
     for (int mt = 0; mt < C::KD; ++mt)
 #pragma unroll
@@ -784,7 +787,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   // [rank * HS / CS, (rank + 1) * HS / CS) of every row over the CS blocks:
   // M = max_c m_c, w_c = 2^(m_c - M), O = sum_c w_c O_c, L = sum_c w_c l_c.
   float* sO = reinterpret_cast<float*>(smem + C::OFF_K);
-  if (warp != C::NWC) {
+  if (warp < C::NWC) {
 #pragma unroll
     for (int mt = 0; mt < C::KD; ++mt)
 #pragma unroll
