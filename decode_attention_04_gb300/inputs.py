@@ -149,10 +149,46 @@ def make_inputs(w: Workload, device="cpu", poison: bool = True, seed: int | None
     return q, k, v, ln
 
 
+E4M3_NAN_CODE = 0x7F
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(cache: torch.Tensor):
+    """A cache writer's FP8 step: one fp32 scale per (sequence, KV head),
+    absmax / 448 over its finite values, and the E4M3 codes of value / scale
+    (round to nearest; NaN stays NaN). Returns (codes uint8 [B,NKV,cap,HS],
+    scales fp32 [B,NKV])."""
+    x = cache.float()
+    finite = torch.isfinite(x)
+    amax = torch.where(finite, x.abs(), torch.zeros_like(x)).amax(dim=(2, 3))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    codes = (x / scale[:, :, None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
+def make_inputs_fp8(w: Workload, device="cpu", poison: bool = True, seed: int | None = None,
+                    lens: torch.Tensor | None = None):
+    """Q (bf16), an FP8 E4M3 K and V cache (uint8 codes) with per-(sequence,
+    KV head) fp32 scales, and lens: the bf16 draw of make_inputs, quantized;
+    slots holding no live position get the NaN code."""
+    q, k, v, ln = make_inputs(w, device=device, poison=False, seed=seed, lens=lens)
+    k8, ks = quantize_e4m3(k)
+    v8, vs = quantize_e4m3(v)
+    del k, v
+    if poison:
+        for b, length in enumerate(ln.tolist()):
+            dead = ~live_slots(int(length), w.capacity, w.window)
+            if dead.any():
+                idx = dead.nonzero().view(-1).to(k8.device)
+                k8[b].index_fill_(1, idx, E4M3_NAN_CODE)
+                v8[b].index_fill_(1, idx, E4M3_NAN_CODE)
+    return q, k8, v8, ks, vs, ln
+
+
 def small(w: Workload, **kw) -> Workload:
     """A copy of a workload with some fields replaced (for scaled-down cases)."""
     return replace(w, **kw)
 
 
-__all__ = ["Workload", "WORKLOADS", "PROFILE_WORKLOADS", "draw_lens", "make_inputs", "live_slots",
-           "poison_dead_slots", "small", "BF16_NAN_BITS"]
+__all__ = ["Workload", "WORKLOADS", "PROFILE_WORKLOADS", "draw_lens", "make_inputs", "make_inputs_fp8",
+           "quantize_e4m3", "live_slots", "poison_dead_slots", "small", "BF16_NAN_BITS", "E4M3_NAN_CODE"]

@@ -57,6 +57,12 @@ def _load():
         lib.fd_oracle_decode_split.argtypes = [u16p, u16p, u16p, i32p, ci, ci, ci, ci, ci, ci,
                                                ctypes.c_double, ci, ci, f64p]
         lib.fd_oracle_decode_split.restype = ci
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.fd_oracle_decode_fp8.argtypes = [u16p, u8p, u8p, f32p, f32p, i32p, ci, ci, ci, ci, ci, ci,
+                                             ctypes.c_double, u8p, ci, f64p]
+        lib.fd_oracle_decode_fp8.restype = ci
+        lib.fd_oracle_e4m3_table.argtypes = [f64p]
+        lib.fd_oracle_e4m3_table.restype = None
         _lib = lib
     return _lib
 
@@ -124,6 +130,51 @@ def decode_split(q, k_cache, v_cache, lens, B, NH, NKV, HS, capacity, window, sc
     return out
 
 
+def _codes(a) -> np.ndarray:
+    """Accept a torch float8_e4m3fn / uint8 tensor or a uint8 numpy array of E4M3 codes."""
+    if not isinstance(a, np.ndarray):
+        import torch
+        t = a.detach().cpu().contiguous()
+        if t.dtype != torch.uint8:
+            t = t.view(torch.uint8)
+        a = t.numpy()
+    assert a.dtype == np.uint8
+    return np.ascontiguousarray(a)
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, lens, B, NH, NKV, HS, capacity, window, scale,
+               want=None, nthreads: int = 0) -> np.ndarray:
+    """FP64 attention output [B, NH, HS] for bf16 q and an E4M3 cache:
+    k8/v8 codes [B,NKV,capacity,HS], k_scale/v_scale fp32 [B,NKV] (value of a
+    code = its E4M3 number x the scale of its (sequence, KV head))."""
+    lib = _load()
+    qb, kc, vc = _bits(q), _codes(k8), _codes(v8)
+    assert qb.size == B * NH * HS and kc.size == B * NKV * capacity * HS and vc.size == kc.size
+    ks = np.ascontiguousarray(np.asarray(k_scale, dtype=np.float32).reshape(-1))
+    vs = np.ascontiguousarray(np.asarray(v_scale, dtype=np.float32).reshape(-1))
+    assert ks.size == B * NKV and vs.size == B * NKV
+    ln = np.ascontiguousarray(np.asarray(lens, dtype=np.int32).reshape(-1))
+    out = np.zeros((B, NH, HS), dtype=np.float64)
+    w = None
+    if want is not None:
+        w = np.ascontiguousarray(np.asarray(want, dtype=np.uint8).reshape(-1))
+    rc = lib.fd_oracle_decode_fp8(_ptr(qb, ctypes.c_uint16), _ptr(kc, ctypes.c_uint8), _ptr(vc, ctypes.c_uint8),
+                                  _ptr(ks, ctypes.c_float), _ptr(vs, ctypes.c_float), _ptr(ln, ctypes.c_int32),
+                                  B, NH, NKV, HS, capacity, window, default_scale(HS, scale),
+                                  None if w is None else _ptr(w, ctypes.c_uint8), nthreads,
+                                  _ptr(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("fd_oracle_decode_fp8: invalid arguments")
+    return out
+
+
+def e4m3_table() -> np.ndarray:
+    """The oracle's value for each of the 256 E4M3 codes."""
+    out = np.zeros(256, dtype=np.float64)
+    _load().fd_oracle_e4m3_table(_ptr(out, ctypes.c_double))
+    return out
+
+
 def bf16_round(x: np.ndarray) -> np.ndarray:
     """Round float64 values to the nearest bf16 (ties to even mantissa) and
     return the bit patterns as uint16. The rounding is taken directly from the
@@ -167,4 +218,5 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-__all__ = ["build", "decode", "decode_split", "default_scale", "bf16_round", "bf16_bits_to_f64"]
+__all__ = ["build", "decode", "decode_split", "decode_fp8", "e4m3_table", "default_scale", "bf16_round",
+           "bf16_bits_to_f64"]

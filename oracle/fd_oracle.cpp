@@ -32,6 +32,15 @@
 // contiguous pieces, keep an unnormalised (O, m, l) per piece, merge) in FP64.
 // It exists so the tests can show that the merge algebra is exact; the plain
 // function above is the oracle proper.
+//
+// A third computes the same attention over an FP8 (E4M3) cache: the same
+// page's section "What we'd tell the next person" says FP8 KV storage needs
+// no special hardware and is dequantised inline ("storage format is not
+// compute format"). Reading taken: K and V are stored as E4M3 codes with one
+// fp32 scale per (sequence, KV head) for K and one for V; the value of a code
+// is its E4M3 number times that scale. E4M3 (1 sign, 4 exponent bits with
+// bias 7, 3 mantissa bits; exponent field 0 = subnormal; code x111_1111 =
+// NaN; no infinity) is decoded from that definition.
 
 #include <algorithm>
 #include <cmath>
@@ -58,7 +67,21 @@ struct Problem {
   int B, NH, NKV, HS, capacity, window;
   double scale;
   const uint8_t* want;  // optional: which (b, h) outputs to compute
+  // FP8 cache (k8/v8 non-null): E4M3 codes and per-(b, kvh) fp32 scales
+  const uint8_t* k8 = nullptr;
+  const uint8_t* v8 = nullptr;
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
 };
+
+// Value of an E4M3 code: (-1)^s * 2^(e-7) * (1 + m/8) for e > 0,
+// (-1)^s * 2^-6 * (m/8) for e = 0, NaN for e = 15 and m = 7.
+double e4m3_to_double(uint8_t code) {
+  const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
 
 // Live band of one sequence: positions [lo, hi).
 void live_band(const Problem& p, int len, int64_t* lo, int64_t* hi) {
@@ -79,6 +102,15 @@ void gather_band(const Problem& p, int b, int kvh, int64_t lo, int64_t hi,
     const int64_t pos = lo + i;
     const int64_t slot = pos % p.capacity;
     const int64_t row = (static_cast<int64_t>(b) * p.NKV + kvh) * p.capacity + slot;
+    if (p.k8) {
+      const double ks = p.k_scale[static_cast<int64_t>(b) * p.NKV + kvh];
+      const double vs = p.v_scale[static_cast<int64_t>(b) * p.NKV + kvh];
+      for (int d = 0; d < p.HS; ++d) {
+        kb[i * p.HS + d] = e4m3_to_double(p.k8[row * p.HS + d]) * ks;
+        vb[i * p.HS + d] = e4m3_to_double(p.v8[row * p.HS + d]) * vs;
+      }
+      continue;
+    }
     for (int d = 0; d < p.HS; ++d) {
       kb[i * p.HS + d] = bf16_bits_to_double(p.k[row * p.HS + d]);
       vb[i * p.HS + d] = bf16_bits_to_double(p.v[row * p.HS + d]);
@@ -182,7 +214,8 @@ void attend_one_split(const Problem& p, int b, int h, int splits, double* out) {
 }
 
 int check_args(const Problem& p, double* out) {
-  if (!p.q || !p.k || !p.v || !p.lens || !out) return 1;
+  if (!p.q || !p.lens || !out) return 1;
+  if (p.k8 ? (!p.v8 || !p.k_scale || !p.v_scale) : (!p.k || !p.v)) return 1;
   if (p.B < 0 || p.NH <= 0 || p.NKV <= 0 || p.HS <= 0 || p.capacity <= 0) return 1;
   if (p.NH % p.NKV != 0) return 1;
   for (int b = 0; b < p.B; ++b)
@@ -222,6 +255,23 @@ int fd_oracle_decode(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   if (check_args(p, out)) return 1;
   for_each_row(p, nthreads, [&](int b, int h) { attend_one(p, b, h, out); });
   return 0;
+}
+
+// The same over an FP8 (E4M3) cache: k8/v8 codes [B][NKV][capacity][HS],
+// k_scale/v_scale fp32 [B][NKV].
+int fd_oracle_decode_fp8(const uint16_t* q, const uint8_t* k8, const uint8_t* v8, const float* k_scale,
+                         const float* v_scale, const int32_t* lens, int B, int NH, int NKV, int HS,
+                         int capacity, int window, double scale, const uint8_t* want, int nthreads,
+                         double* out) {
+  Problem p{q, nullptr, nullptr, lens, B, NH, NKV, HS, capacity, window, scale, want, k8, v8, k_scale, v_scale};
+  if (check_args(p, out)) return 1;
+  for_each_row(p, nthreads, [&](int b, int h) { attend_one(p, b, h, out); });
+  return 0;
+}
+
+// Value of every E4M3 code 0..255 (for the tests' decoding pin).
+void fd_oracle_e4m3_table(double* out256) {
+  for (int c = 0; c < 256; ++c) out256[c] = e4m3_to_double(static_cast<uint8_t>(c));
 }
 
 // FP64 restatement of the split form with `splits` near-equal pieces.

@@ -274,3 +274,64 @@ def test_sampled_rows_equal_full(oracle_mod):
             assert np.array_equal(part[b, h], full[b, h])
         else:
             assert not part[b, h].any()
+
+
+# ------------------------------------------------------- FP8 (E4M3) cache form
+
+def test_e4m3_decoding_matches_library_for_every_code(oracle_mod):
+    """The oracle's E4M3 values (from the format's definition) equal torch's
+    float8_e4m3fn conversion for all 256 codes, NaN codes included."""
+    ours = oracle_mod.e4m3_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ours)
+    assert np.array_equal(ours[fin], ref[fin])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9  # largest finite, smallest subnormal
+
+
+def _fp8_case(spec, seed):
+    from decode_attention_04_gb300.inputs import make_inputs_fp8
+    B, NH, NKV, HS, cap, win, lens = spec
+    w = Workload("tiny8", B, NH, NKV, HS, cap, win, lens=lens, seed=seed)
+    return (w, *make_inputs_fp8(w))
+
+
+@pytest.mark.parametrize("spec", TINY[:6])
+def test_fp8_form_equals_bf16_form_on_exact_values(spec, oracle_mod):
+    """With power-of-two scales every dequantised value is a bf16 value; the
+    FP8 form must then give exactly the bf16 oracle's result."""
+    w, q, k8, v8, ks, vs, ln = _fp8_case(spec, seed=31)
+    ks = torch.full_like(ks, 2.0 ** -5)
+    vs = torch.full_like(vs, 2.0 ** 3)
+    table = torch.tensor(oracle_mod.e4m3_table())
+    kd = (table[k8.long()] * 2.0 ** -5).to(torch.bfloat16)
+    vd = (table[v8.long()] * 2.0 ** 3).to(torch.bfloat16)
+    assert torch.equal(kd.double().nan_to_num(7.0), (table[k8.long()] * 2.0 ** -5).nan_to_num(7.0))
+    d = _wdict(w)
+    got = oracle_mod.decode_fp8(q, k8, v8, ks, vs, ln, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    ref = _run(oracle_mod, q, kd, vd, ln, d)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("spec", TINY[:6])
+def test_fp8_form_equals_sdpa_on_dequantised_values(spec, oracle_mod):
+    """Arbitrary per-(sequence, KV head) scales: the FP8 form equals torch SDPA
+    (float64) over the dequantised cache, to 1e-12."""
+    w, q, k8, v8, ks, vs, ln = _fp8_case(spec, seed=32)
+    table = torch.tensor(oracle_mod.e4m3_table())
+    kd = table[k8.long()] * ks.double()[:, :, None, None]
+    vd = table[v8.long()] * vs.double()[:, :, None, None]
+    got = oracle_mod.decode_fp8(q, k8, v8, ks, vs, ln, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    assert np.isfinite(got).all()  # the NaN codes sit outside the band
+    G = w.NH // w.NKV
+    for b in range(w.B):
+        L = int(ln[b])
+        if L == 0:
+            assert not got[b].any()
+            continue
+        keep = min(w.window if w.window > 0 else w.capacity, w.capacity)
+        pos = torch.arange(max(0, L - keep), L)
+        kk = kd[b][:, pos % w.capacity].repeat_interleave(G, dim=0)
+        vv = vd[b][:, pos % w.capacity].repeat_interleave(G, dim=0)
+        o = torch.nn.functional.scaled_dot_product_attention(q[b].double().unsqueeze(1), kk, vv, scale=w.scale)
+        np.testing.assert_allclose(got[b], o[:, 0].numpy(), rtol=0, atol=1e-12)
