@@ -1,5 +1,5 @@
 """Python binding of libfd.so: single-token split-KV decode attention
-(Flash-Decoding) over a position-addressed bf16 KV cache on GB300.
+(Flash-Decoding) over a position-addressed bf16 or FP8 (E4M3) KV cache on GB300.
 
 Every function here has the name of the C entry point it wraps
 (include/fd_decode_attn.h) and only marshals arguments: torch tensors become
@@ -33,9 +33,12 @@ FD_PATH_AUTO = 0
 FD_PATH_SIMT = 1
 FD_PATH_TC = 2
 
-EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_override", "fd_workspace_bytes", "fd_decode_attn",
-            "fd_decode_attn_ex", "fd_decode_attn_noalloc", "fd_get_device_error", "fd_release", "fd_strerror",
-            "fd_version"]
+FD_KV_BF16 = 0
+FD_KV_E4M3 = 1
+
+EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_kv", "fd_plan_sms_kv", "fd_plan_override", "fd_workspace_bytes",
+            "fd_decode_attn", "fd_decode_attn_ex", "fd_decode_attn_fp8", "fd_decode_attn_fp8_ex",
+            "fd_decode_attn_noalloc", "fd_get_device_error", "fd_release", "fd_strerror", "fd_version"]
 
 
 class fd_plan_t(ctypes.Structure):
@@ -50,6 +53,7 @@ class fd_plan_t(ctypes.Structure):
         ("max_cluster", ctypes.c_int),
         ("fused", ctypes.c_int),
         ("group_bytes", ctypes.c_int),
+        ("kv_dtype", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("workspace_zero_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),
@@ -88,11 +92,16 @@ def load_library(path: Path | str | None = None):
     sig = {
         "fd_plan": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_sms": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
+        "fd_plan_kv": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
+        "fd_plan_sms_kv": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_override": (ci, [planp, ci, ci, ci, ci]),
         "fd_workspace_bytes": (sz, [planp]),
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
                                    ctypes.c_float, vp]),
+        "fd_decode_attn_fp8": (ci, [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
+        "fd_decode_attn_fp8_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
+                                       ctypes.c_float, vp]),
         "fd_decode_attn_noalloc": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_get_device_error": (ci, [vp, ctypes.POINTER(ctypes.c_uint)]),
         "fd_release": (None, []),
@@ -154,6 +163,24 @@ def fd_plan_sms(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm,
     return p
 
 
+def fd_plan_kv(B, NH, NKV, HS, capacity, window, max_len=0, device=None, kv_dtype=FD_KV_BF16) -> fd_plan_t:
+    if device is None:
+        import torch
+        device = torch.cuda.current_device()
+    p = fd_plan_t()
+    _check(load_library().fd_plan_kv(B, NH, NKV, HS, capacity, window, max_len, int(device), int(kv_dtype),
+                                     ctypes.byref(p)), "fd_plan_kv")
+    return p
+
+
+def fd_plan_sms_kv(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, max_cluster=8,
+                   kv_dtype=FD_KV_BF16) -> fd_plan_t:
+    p = fd_plan_t()
+    _check(load_library().fd_plan_sms_kv(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm,
+                                         max_cluster, int(kv_dtype), ctypes.byref(p)), "fd_plan_sms_kv")
+    return p
+
+
 def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_AUTO, cluster: int = 0,
                      fused: int = -1) -> fd_plan_t:
     _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path, cluster, fused),
@@ -179,6 +206,23 @@ def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k
                                             _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
                                             _stream(stream)),
            "fd_decode_attn_ex")
+
+
+def fd_decode_attn_fp8(q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, capacity, window, scale,
+                       stream=None) -> None:
+    _check(load_library().fd_decode_attn_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                             _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
+                                             _stream(stream)),
+           "fd_decode_attn_fp8")
+
+
+def fd_decode_attn_fp8_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k8, v8, k_scale, v_scale, out,
+                          lens, B, NH, NKV, HS, capacity, window, scale, stream=None) -> None:
+    _check(load_library().fd_decode_attn_fp8_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
+                                                _ptr(out_f32), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                                                _ptr(v_scale), _ptr(out), _ptr(lens), B, NH, NKV, HS, capacity,
+                                                window, float(scale), _stream(stream)),
+           "fd_decode_attn_fp8_ex")
 
 
 def fd_decode_attn_noalloc(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale,

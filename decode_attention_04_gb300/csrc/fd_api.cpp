@@ -76,6 +76,7 @@ int fused_rule(const fd_plan_t& p) {
 // 4 KB copy groups (a tile that needs the whole SM) only for the head-dim-512,
 // 16-row tile, and only when the grid fits one wave at one block per SM.
 int group_rule(const fd_plan_t& p) {
+  if (p.kv_dtype == FD_KV_E4M3) return 1024;  // E4M3 tiles: the same positions, half the bytes
   const long long G = p.NH / p.NKV;
   const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
@@ -88,6 +89,10 @@ void finish_plan(fd_plan_t* p, int fused = -1) {
   p->workspace_zero_bytes = ws_counter_bytes(*p);
 }
 
+bool valid_kv(int kv_dtype, int path) {
+  return kv_dtype == FD_KV_BF16 || (kv_dtype == FD_KV_E4M3 && path == FD_PATH_TC);
+}
+
 bool valid_cluster(int cluster, int num_splits, int HS, int path) {
   if (cluster < 1 || cluster > 16 || (cluster & (cluster - 1)) != 0) return false;
   if (num_splits % cluster != 0 || (HS / cluster) % 4 != 0) return false;
@@ -96,13 +101,15 @@ bool valid_cluster(int cluster, int num_splits, int HS, int path) {
 
 // The split rule, documented in fd_decode_attn.h beside fd_plan_t.
 int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
-              int ctas_per_sm, int max_cluster, int path, fd_plan_t* plan) {
+              int ctas_per_sm, int max_cluster, int path, int kv_dtype, fd_plan_t* plan) {
   if (!plan) return FD_ERR_INVALID_ARG;
   int rc = check_shape(B, NH, NKV, HS, capacity, window);
   if (rc != FD_OK) return rc;
   if (num_sms <= 0 || ctas_per_sm <= 0 || max_cluster < 1) return FD_ERR_INVALID_ARG;
   if (path == FD_PATH_AUTO) path = FD_PATH_TC;
   if (path != FD_PATH_TC && path != FD_PATH_SIMT) return FD_ERR_INVALID_ARG;
+  if (kv_dtype != FD_KV_BF16 && kv_dtype != FD_KV_E4M3) return FD_ERR_INVALID_ARG;
+  if (!valid_kv(kv_dtype, path)) return FD_ERR_UNSUPPORTED;
 
   const int keep = window > 0 ? window : capacity;
   int max_band = keep < capacity ? keep : capacity;
@@ -126,7 +133,8 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   long long chunk = chunk_for(s_fill);
   // Balance bound: at most ~2 MiB of K+V per split, so a ragged batch does not
   // leave a few long splits running alone at the end.
-  const long long max_chunk = std::max<long long>(granule, (2ll << 20) / (4ll * HS));
+  const long long pos_bytes = (kv_dtype == FD_KV_E4M3 ? 2ll : 4ll) * HS;  // K + V bytes per position
+  const long long max_chunk = std::max<long long>(granule, (2ll << 20) / pos_bytes);
   long long S = (max_band + chunk - 1) / chunk;
   if (chunk > max_chunk) {
     long long waves = (static_cast<long long>(max_band) + max_chunk * s_fill - 1) / (max_chunk * s_fill);
@@ -158,6 +166,7 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   p.HS = HS;
   p.capacity = capacity;
   p.window = window;
+  p.kv_dtype = kv_dtype;
   finish_plan(&p);
   *plan = p;
   return FD_OK;
@@ -223,13 +232,18 @@ int get_workspace(int device, cudaStream_t stream, size_t need, void** ptr) {
   return FD_OK;
 }
 
+// k_scale / v_scale are null for a bf16 cache; for an E4M3 cache k_cache and
+// v_cache hold the codes.
 int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* out_f32, const void* q,
-        const void* k_cache, const void* v_cache, void* out, const int* lens, float scale,
-        cudaStream_t stream) {
+        const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale, void* out,
+        const int* lens, float scale, cudaStream_t stream) {
   if (plan.B == 0) return FD_OK;
+  const bool kv8 = plan.kv_dtype == FD_KV_E4M3;
   if (!q || !k_cache || !v_cache || !out || !lens) return FD_ERR_INVALID_ARG;
+  if (kv8 && (!k_scale || !v_scale)) return FD_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-      !aligned(lens, 4) || (out_f32 && !aligned(out_f32, 16)))
+      !aligned(lens, 4) || (out_f32 && !aligned(out_f32, 16)) ||
+      (kv8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))))
     return FD_ERR_ALIGNMENT;
   const size_t need = ws_total(plan);
   if (need > 0) {
@@ -240,8 +254,16 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
 
   fd::LaunchArgs a{};
   a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(k_cache);
-  a.v = static_cast<const uint16_t*>(v_cache);
+  a.kv8 = kv8 ? 1 : 0;
+  if (kv8) {
+    a.k8 = static_cast<const uint8_t*>(k_cache);
+    a.v8 = static_cast<const uint8_t*>(v_cache);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+  } else {
+    a.k = static_cast<const uint16_t*>(k_cache);
+    a.v = static_cast<const uint16_t*>(v_cache);
+  }
   a.out = static_cast<uint16_t*>(out);
   a.out_f32 = out_f32;
   a.lens = lens;
@@ -272,11 +294,18 @@ extern "C" {
 int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
                 int ctas_per_sm, int max_cluster, fd_plan_t* plan) {
   return make_plan(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, max_cluster, FD_PATH_AUTO,
-                   plan);
+                   FD_KV_BF16, plan);
 }
 
-int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int device,
-            fd_plan_t* plan) {
+int fd_plan_sms_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int num_sms,
+                   int ctas_per_sm, int max_cluster, int kv_dtype, fd_plan_t* plan) {
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, num_sms, ctas_per_sm, max_cluster, FD_PATH_AUTO,
+                   kv_dtype, plan);
+}
+
+int fd_plan_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int device, int kv_dtype,
+               fd_plan_t* plan) {
+  if (kv_dtype != FD_KV_BF16 && kv_dtype != FD_KV_E4M3) return FD_ERR_INVALID_ARG;
   if (!plan) return FD_ERR_INVALID_ARG;
   int rc = check_shape(B, NH, NKV, HS, capacity, window);
   if (rc != FD_OK) return rc;
@@ -287,11 +316,18 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
   if (cudaGetDevice(&prev) != cudaSuccess) return FD_ERR_CUDA;
   if (prev != device && cudaSetDevice(device) != cudaSuccess) return FD_ERR_CUDA;
   int ctas = 0, max_cluster = 1;
-  cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, NH / NKV, &ctas);
-  if (e == cudaSuccess) e = fd::query_max_cluster(HS, NH / NKV, &max_cluster);
+  const bool kv8 = kv_dtype == FD_KV_E4M3;
+  cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, NH / NKV, kv8, &ctas);
+  if (e == cudaSuccess) e = fd::query_max_cluster(HS, NH / NKV, kv8, &max_cluster);
   if (prev != device) cudaSetDevice(prev);
   if (e != cudaSuccess || ctas <= 0) return FD_ERR_CUDA;
-  return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, max_cluster, FD_PATH_AUTO, plan);
+  return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, max_cluster, FD_PATH_AUTO, kv_dtype,
+                   plan);
+}
+
+int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_len, int device,
+            fd_plan_t* plan) {
+  return fd_plan_kv(B, NH, NKV, HS, capacity, window, max_len, device, FD_KV_BF16, plan);
 }
 
 int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int fused) {
@@ -304,6 +340,7 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
     p.path = path;
     p.granule = fd::plan_granule(path, p.HS);
   }
+  if (!valid_kv(p.kv_dtype, p.path)) return FD_ERR_INVALID_ARG;  // E4M3 runs on the tensor-core path only
   if (num_splits > 0) p.num_splits = num_splits;
   if (cluster > 0) p.cluster = cluster;
   if (p.path == FD_PATH_SIMT && cluster == 0) p.cluster = 1;  // the SIMT path has no clusters
@@ -316,42 +353,88 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
 
 size_t fd_workspace_bytes(const fd_plan_t* plan) { return plan ? ws_total(*plan) : 0; }
 
-int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes, float* out_f32,
-                      const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens,
-                      int B, int NH, int NKV, int HS, int capacity, int window, float scale,
-                      fd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// A plan is usable for this call: it was made for these sizes and this cache
+// type, and its fields are self-consistent.
+int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int HS, int capacity, int window) {
   if (!plan) return FD_ERR_INVALID_ARG;
   int rc = check_shape(B, NH, NKV, HS, capacity, window);
   if (rc != FD_OK) return rc;
   if (plan->B != B || plan->NH != NH || plan->NKV != NKV || plan->HS != HS || plan->capacity != capacity ||
-      plan->window != window)
+      plan->window != window || plan->kv_dtype != kv_dtype)
     return FD_ERR_INVALID_ARG;
   if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1 ||
-      !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
-      (plan->fused && !fused_rule_allowed(*plan)) || (plan->group_bytes != 2048 && plan->group_bytes != 4096) ||
+      !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
+      (plan->fused && !fused_rule_allowed(*plan)))
+    return FD_ERR_INVALID_ARG;
+  if (kv_dtype == FD_KV_E4M3) return plan->group_bytes == 1024 ? FD_OK : FD_ERR_INVALID_ARG;
+  if ((plan->group_bytes != 2048 && plan->group_bytes != 4096) ||
       (plan->group_bytes == 4096 && group_rule(*plan) != 4096 &&
        !(plan->HS == 512 && plan->NH / plan->NKV > 8 && plan->path == FD_PATH_TC)))
     return FD_ERR_INVALID_ARG;
-  return run(*plan, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens, scale,
-             reinterpret_cast<cudaStream_t>(stream));
+  return FD_OK;
 }
 
-int fd_decode_attn(const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens, int B,
-                   int NH, int NKV, int HS, int capacity, int window, float scale, fd_stream_t stream) {
+// Plan for the current device, take the library's workspace for this
+// (device, stream), then run.
+int run_auto(int kv_dtype, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+             const float* v_scale, void* out, const int* lens, int B, int NH, int NKV, int HS, int capacity,
+             int window, float scale, fd_stream_t stream) {
   int rc = check_shape(B, NH, NKV, HS, capacity, window);
   if (rc != FD_OK) return rc;
   if (B == 0) return FD_OK;
   if (!q || !k_cache || !v_cache || !out || !lens) return FD_ERR_INVALID_ARG;
+  if (kv_dtype == FD_KV_E4M3 && (!k_scale || !v_scale)) return FD_ERR_INVALID_ARG;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return FD_ERR_CUDA;
   fd_plan_t plan;
-  rc = fd_plan(B, NH, NKV, HS, capacity, window, 0, device, &plan);
+  rc = fd_plan_kv(B, NH, NKV, HS, capacity, window, 0, device, kv_dtype, &plan);
   if (rc != FD_OK) return rc;
   void* ws = nullptr;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   rc = get_workspace(device, s, plan.workspace_bytes, &ws);
   if (rc != FD_OK) return rc;
-  return run(plan, ws, plan.workspace_bytes, nullptr, q, k_cache, v_cache, out, lens, scale, s);
+  return run(plan, ws, plan.workspace_bytes, nullptr, q, k_cache, v_cache, k_scale, v_scale, out, lens, scale, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes, float* out_f32,
+                      const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens,
+                      int B, int NH, int NKV, int HS, int capacity, int window, float scale,
+                      fd_stream_t stream) {
+  const int rc = check_plan(plan, FD_KV_BF16, B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  return run(*plan, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, nullptr, nullptr, out, lens, scale,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fd_decode_attn(const void* q, const void* k_cache, const void* v_cache, void* out, const int* lens, int B,
+                   int NH, int NKV, int HS, int capacity, int window, float scale, fd_stream_t stream) {
+  return run_auto(FD_KV_BF16, q, k_cache, v_cache, nullptr, nullptr, out, lens, B, NH, NKV, HS, capacity, window,
+                  scale, stream);
+}
+
+int fd_decode_attn_fp8_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes, float* out_f32,
+                          const void* q, const void* k8, const void* v8, const float* k_scale,
+                          const float* v_scale, void* out, const int* lens, int B, int NH, int NKV, int HS,
+                          int capacity, int window, float scale, fd_stream_t stream) {
+  const int rc = check_plan(plan, FD_KV_E4M3, B, NH, NKV, HS, capacity, window);
+  if (rc != FD_OK) return rc;
+  return run(*plan, workspace, workspace_bytes, out_f32, q, k8, v8, k_scale, v_scale, out, lens, scale,
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fd_decode_attn_fp8(const void* q, const void* k8, const void* v8, const float* k_scale, const float* v_scale,
+                       void* out, const int* lens, int B, int NH, int NKV, int HS, int capacity, int window,
+                       float scale, fd_stream_t stream) {
+  return run_auto(FD_KV_E4M3, q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, capacity, window, scale,
+                  stream);
 }
 
 int fd_get_device_error(fd_stream_t stream, unsigned int* err) {

@@ -23,6 +23,11 @@ struct LaunchArgs {
   unsigned int* counters;   // [B][NKV] finished-split counters (fused merge), zero between calls
   int fused;                // 1: the last split block of each (b, kvh) merges; no merge kernel
   int group_bytes;          // bytes per bulk-copy group of the tile (2048, or 4096 for the wide MQA tile)
+  int kv8;                  // 1: the cache is E4M3 codes (k8/v8) with per-(b, kvh) scales
+  const uint8_t* k8;        // E4M3 [B][NKV][capacity][HS]  (kv8 only)
+  const uint8_t* v8;        // E4M3 [B][NKV][capacity][HS]  (kv8 only)
+  const float* k_scale;     // fp32 [B][NKV]                 (kv8 only)
+  const float* v_scale;     // fp32 [B][NKV]                 (kv8 only)
   int B, NH, NKV, HS, capacity, window;  // window <= 0: none
   int num_splits;           // S
   int cluster;              // blocks per cluster along the splits (S % cluster == 0)
@@ -37,11 +42,11 @@ int tc_tile_positions(int HS);
 int plan_granule(int path, int HS);
 
 // Resident CTAs per SM of the kernel a plan would launch (occupancy query).
-cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas);
+cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas);
 
 // Largest cluster size (16, 8, ... 1) of the tensor-core split kernel that the
 // device can schedule (cluster occupancy query).
-cudaError_t query_max_cluster(int HS, int G, int* cluster);
+cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster);
 
 // Launch the split kernel (and the merge kernel when S > 1) on `stream`.
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);

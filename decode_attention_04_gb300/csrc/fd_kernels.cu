@@ -22,6 +22,8 @@
 //   merge_kernel       online-softmax merge of the S partials of each row.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cstdint>
 #include <utility>
 
@@ -230,6 +232,28 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D += A(16x16, row) * B(16x8, col), fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte = first element) to an fp16 pair (low half = first),
+// exactly: every E4M3 value, subnormals included, is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+}
+
 // ======================================================= SIMT reference kernel
 
 constexpr int kSimtThreads = 128;
@@ -352,8 +376,14 @@ size_t simt_smem_bytes(int G, int HS) {
 // i.e. in eight different 16-byte bank groups, so every 8-row ldmatrix is
 // conflict-free. Scores, P and the P.V contraction all use the same order;
 // the softmax does not depend on the order of positions.
-template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048>
+//
+// E4M3 caches (KV8): the ring holds the codes in 1 KB groups (the same tile
+// positions as the bf16 tile, half the bytes); the consumers widen each
+// arrived stage into one fp16 tile laid out as the bf16 tile is, and release
+// the stage at once, so the copies of later tiles overlap the MMAs.
+template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048, bool KV8_ = false>
 struct TcCfg {
+  static constexpr bool KV8 = KV8_;
   static constexpr int HS = HS_;
   static constexpr int NT = NT_;          // 8-row tiles of query rows (G <= 8 * NT)
   static constexpr int NP = 8 * NT;       // padded query rows
@@ -373,10 +403,17 @@ struct TcCfg {
   static constexpr int TPR = CTHREADS / NP;  // softmax threads per query row
   static constexpr int PPT = T / TPR;        // positions per softmax thread
   static constexpr size_t STAGE_BYTES = static_cast<size_t>(NG) * GP;
+  // compute-layout tiles held: the copy ring itself (bf16), or one widened tile (KV8)
+  static constexpr int NBUF = KV8 ? 1 : NSTAGE;
+  static constexpr int ROWB8 = HS;                // bytes of one E4M3 cache row
+  static constexpr int GP8 = R * ROWB8 + 16;      // E4M3 group pitch, bytes
+  static constexpr size_t STAGE8_BYTES = KV8 ? static_cast<size_t>(NG) * GP8 : 0;
   static constexpr size_t OFF_K = 0;
-  static constexpr size_t OFF_V = OFF_K + NSTAGE * STAGE_BYTES;
+  static constexpr size_t OFF_V = OFF_K + NBUF * STAGE_BYTES;
+  static constexpr size_t OFF_K8 = OFF_V + NBUF * STAGE_BYTES;   // E4M3 copy ring (KV8 only)
+  static constexpr size_t OFF_V8 = OFF_K8 + NSTAGE * STAGE8_BYTES;
   static constexpr int SP = T + 4;       // score row pitch (floats): conflict-free stores and loads
-  static constexpr size_t OFF_S = OFF_V + NSTAGE * STAGE_BYTES;              // f32 [NWC][NP][SP]
+  static constexpr size_t OFF_S = OFF_V8 + NSTAGE * STAGE8_BYTES;            // f32 [NWC][NP][SP]
   static constexpr size_t OFF_P = OFF_S + static_cast<size_t>(NWC) * NP * SP * 4;  // bf16 [2][NP][PPITCH]
   static constexpr size_t OFF_A = OFF_P + static_cast<size_t>(2) * NP * PPITCH * 2;  // f32 alpha,m,l [NP]
   static constexpr size_t OFF_BAR = (OFF_A + 3 * NP * 4 + 7) / 8 * 8;        // u64 full[], empty[]
@@ -396,8 +433,10 @@ struct TcCfg {
   static_assert(TPR <= 32 && 32 % TPR == 0, "a row's softmax threads must sit in one warp");
   static_assert(ROWB % 16 == 0 && GP % 16 == 0, "bulk copies need 16-byte granules");
   static_assert(NG <= 32, "one producer lane per group");
-  // cluster reduction: O parked in the K stages, weights in the score buffer
-  static_assert(static_cast<size_t>(NP) * HS * 4 <= NSTAGE * STAGE_BYTES, "O must fit the K stages");
+  // cluster reduction: O parked in the tile buffers (all of [0, OFF_S) is idle
+  // once the last tile is consumed), weights in the score buffer
+  static_assert(static_cast<size_t>(NP) * HS * 4 <= OFF_S, "O must fit the tile buffers");
+  static_assert(!KV8 || (GP8 % 16 == 0 && R * ROWB8 == 1024), "E4M3 groups are 1 KB, 16-byte aligned");
   static_assert(NP * 16 + 2 * NP <= NWC * NP * SP, "cluster weights must fit the score buffer");
   static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
@@ -481,31 +520,37 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     // block's copy rate (a block's rate is set by the copies it issues).
     const bool is_k = warp == C::NWC;
     const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
-    const uint16_t* src = (is_k ? a.k : a.v) + head_row0 * C::HS;
+    // byte source of this warp's tensor, and the byte geometry of its ring
+    const unsigned char* src =
+        C::KV8 ? (is_k ? a.k8 : a.v8) + head_row0 * C::HS
+               : reinterpret_cast<const unsigned char*>((is_k ? a.k : a.v) + head_row0 * C::HS);
+    constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
+    constexpr int kGroupPitch = C::KV8 ? C::GP8 : C::GP;
+    constexpr size_t kStageBytes = C::KV8 ? C::STAGE8_BYTES : C::STAGE_BYTES;
+    const size_t ring = C::KV8 ? (is_k ? C::OFF_K8 : C::OFF_V8) : (is_k ? C::OFF_K : C::OFF_V);
     bool failed = false;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::NSTAGE;
       if (i >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((i / C::NSTAGE) - 1) & 1, failed);
       const int nv = min(C::T, n - i * C::T);
       const long long pbase = p0 + static_cast<long long>(i) * C::T;
-      const uint32_t dst =
-          smem_u32(smem + (is_k ? C::OFF_K : C::OFF_V) + static_cast<size_t>(st) * C::STAGE_BYTES);
+      const uint32_t dst = smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes);
       const uint32_t fb = full0 + 8 * st;
       // lane g copies group g: rows [g*R, g*R + rows) of the tile
       const int g = lane;
       const int j0 = g * C::R;
       const int rows = (g < C::NG && j0 < nv) ? min(C::R, nv - j0) : 0;
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * C::ROWB);
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * kRowBytes);
       if (rows > 0) {
         const long long pos0 = pbase + j0;
         const size_t slot0 = static_cast<size_t>(pos0 % a.capacity);
-        const uint32_t goff = static_cast<uint32_t>(g) * C::GP;
+        const uint32_t goff = static_cast<uint32_t>(g) * kGroupPitch;
         if (rows == C::R && slot0 + C::R <= static_cast<size_t>(a.capacity)) {
-          bulk_g2s(dst + goff, src + slot0 * C::HS, C::R * C::ROWB, fb);
+          bulk_g2s(dst + goff, src + slot0 * kRowBytes, C::R * kRowBytes, fb);
         } else {  // a partial group, or one that wraps around the ring: row by row
           for (int r = 0; r < rows; ++r) {
             const size_t slot = static_cast<size_t>((pos0 + r) % a.capacity);
-            bulk_g2s(dst + goff + r * C::ROWB, src + slot * C::HS, C::ROWB, fb);
+            bulk_g2s(dst + goff + r * kRowBytes, src + slot * kRowBytes, kRowBytes, fb);
           }
         }
       }
@@ -531,6 +576,43 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       qf[ks][nt][1] = x1;
     }
 
+  float sl2 = a.scale_log2;  // score scale, log2 units
+  if constexpr (C::KV8) {
+    // fp16 MMAs: Q goes to fp16 with one power-of-two scale per block, so the
+    // block's largest |q| lands in [2^13, 2^14) and no product can overflow;
+    // that scale and the K dequantisation scale fold into the score scale.
+    __shared__ float s_qmax[C::NWC];
+    float qmax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < C::KD; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t x = qf[ks][nt][e];
+          qmax = fmaxf(qmax, fmaxf(fabsf(bf16_bits_to_f32(static_cast<uint16_t>(x & 0xffffu))),
+                                   fabsf(bf16_bits_to_f32(static_cast<uint16_t>(x >> 16)))));
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+    if (lane == 0) s_qmax[warp] = qmax;
+    named_bar_sync(1, C::CTHREADS);
+#pragma unroll
+    for (int w = 0; w < C::NWC; ++w) qmax = fmaxf(qmax, s_qmax[w]);
+    const int eq = (qmax > 0.f && qmax <= 3.0e38f) ? 13 - ilogbf(qmax) : 0;
+#pragma unroll
+    for (int ks = 0; ks < C::KD; ++ks)
+#pragma unroll
+      for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const uint32_t x = qf[ks][nt][e];
+          qf[ks][nt][e] = pack_f16x2(ldexpf(bf16_bits_to_f32(static_cast<uint16_t>(x & 0xffffu)), eq),
+                                     ldexpf(bf16_bits_to_f32(static_cast<uint16_t>(x >> 16)), eq));
+        }
+    sl2 = a.scale_log2 * a.k_scale[static_cast<size_t>(b) * a.NKV + kvh] * ldexpf(1.f, -eq);
+  }
+
   float m_run = kNegInf, l_run = 0.f;
 
   // ldmatrix lane addressing
@@ -541,8 +623,34 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     const int st = i % C::NSTAGE;
     mbar_wait(full0 + 8 * st, (i / C::NSTAGE) & 1, failed);
     const int nv = min(C::T, n - i * C::T);  // valid tile positions: [0, nv)
-    const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES;
-    unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
+    const int buf = C::KV8 ? 0 : st;
+    const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(buf) * C::STAGE_BYTES;
+    unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(buf) * C::STAGE_BYTES;
+    if constexpr (C::KV8) {
+      // E4M3 stage -> fp16 tile, 8 codes per step (positions >= nv become
+      // zeros, so a 0-weight position contributes exactly 0); then the stage
+      // goes back to the producers.
+      if (i > 0) named_bar_sync(1, C::CTHREADS);  // every consumer is done with the previous tile
+      const unsigned char* fK = smem + C::OFF_K8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
+      const unsigned char* fV = smem + C::OFF_V8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
+      constexpr int CH = C::HS / 8;  // 8-code chunks per row
+      for (int w8 = tid; w8 < 2 * C::T * CH; w8 += C::CTHREADS) {
+        const int tensor = w8 / (C::T * CH), rem = w8 % (C::T * CH);
+        const int j = rem / CH, c = rem % CH;
+        uint4 h = make_uint4(0, 0, 0, 0);
+        if (j < nv) {
+          const uint2 codes = *reinterpret_cast<const uint2*>((tensor ? fV : fK) + (j / C::R) * C::GP8 +
+                                                              (j % C::R) * C::ROWB8 + c * 8);
+          h = make_uint4(e4m3x2_to_f16x2(codes.x & 0xffffu), e4m3x2_to_f16x2(codes.x >> 16),
+                         e4m3x2_to_f16x2(codes.y & 0xffffu), e4m3x2_to_f16x2(codes.y >> 16));
+        }
+        unsigned char* dstp = (tensor ? tV : const_cast<unsigned char*>(tK)) + C::off_pos(j) + c * 16;
+        *reinterpret_cast<uint4*>(dstp) = h;
+      }
+      named_bar_sync(1, C::CTHREADS);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
 
     // ---- scores: S^T[m][row] partial over this warp's dims (m = MMA row order)
     float* myS = sS + static_cast<size_t>(warp) * C::NP * C::SP;
@@ -562,7 +670,12 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
           uint32_t a0, a1, a2, a3;
           ldsm_x4(smem_u32(tK + C::off_of(m) + dcol * 2), a0, a1, a2, a3);
 #pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+          for (int nt = 0; nt < C::NT; ++nt) {
+            if constexpr (C::KV8)
+              mma_f16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+            else
+              mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+          }
         }
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
@@ -591,7 +704,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
           float acc = 0.f;
 #pragma unroll
           for (int w = 0; w < C::NWC; ++w) acc += sS[(static_cast<size_t>(w) * C::NP + sr) * C::SP + j];
-          x = acc * a.scale_log2;
+          x = acc * sl2;
         }
         sv[t] = x;
         tmax = fmaxf(tmax, x);
@@ -611,10 +724,14 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       for (int t = 0; t < C::PPT; ++t) {
         const int j = sj + t * C::TPR;
         const float p = exp2f(sv[t] - m_new);
-        const uint16_t hi = f32_to_bf16_bits(p);
-        const uint16_t lo16 = f32_to_bf16_bits(p - bf16_bits_to_f32(hi));
-        phi[j] = hi;
-        plo[j] = lo16;
+        if constexpr (C::KV8) {
+          phi[j] = __half_as_ushort(__float2half_rn(p));  // fp16 P: 11 bits, no second pass
+        } else {
+          const uint16_t hi = f32_to_bf16_bits(p);
+          const uint16_t lo16 = f32_to_bf16_bits(p - bf16_bits_to_f32(hi));
+          phi[j] = hi;
+          plo[j] = lo16;
+        }
         psum += p;
       }
 #pragma unroll
@@ -625,7 +742,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
     // V rows of positions [nv, T) were not written by this tile's copies:
     // zero them so 0-weight positions contribute exactly 0.
-    if (nv < C::T) {
+    if (!C::KV8 && nv < C::T) {
       const int words = (C::T - nv) * (C::HS / 8);  // 16-byte words
       for (int w16 = tid; w16 < words; w16 += C::CTHREADS) {
         const int r = nv + w16 / (C::HS / 8), c = (w16 % (C::HS / 8)) * 16;
@@ -666,16 +783,31 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
           ldsm_x4_trans(smem_u32(tV + C::off_of(m) + dcol * 2), v0, v1, v2, v3);
 #pragma unroll
           for (int nt = 0; nt < C::NT; ++nt) {
-            mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
-            mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][2], pb[nt][3]);
+            if constexpr (C::KV8) {
+              mma_f16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+            } else {
+              mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
+              mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][2], pb[nt][3]);
+            }
           }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    if constexpr (!C::KV8) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
   }
 
+    if constexpr (C::KV8) {  // O in dequantised units: times this head's V scale
+      const float vs = a.v_scale[static_cast<size_t>(b) * a.NKV + kvh];
+#pragma unroll
+      for (int mt = 0; mt < C::KD; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nt][e] *= vs;
+    }
     if (sr < G && sj == 0) {
       sM[sr] = m_run;
       sL[sr] = l_run;
@@ -1006,10 +1138,29 @@ using Tc256x2 = TcCfg<256, 2, 4, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;
 using Tc512x2 = TcCfg<512, 2, 4, 3>;
 using Tc512x2w = TcCfg<512, 2, 4, 3, 4096>;  // one block per SM, 4 KB copies
+// E4M3 caches: 1 KB copy groups (the same tile positions as the bf16 tiles),
+// a three-stage E4M3 ring and one fp16 tile.
+using Tc64x1f = TcCfg<64, 1, 4, 3, 2048, true>;
+using Tc64x2f = TcCfg<64, 2, 4, 3, 2048, true>;
+using Tc128x1f = TcCfg<128, 1, 4, 3, 2048, true>;
+using Tc128x2f = TcCfg<128, 2, 4, 3, 2048, true>;
+using Tc256x1f = TcCfg<256, 1, 4, 3, 2048, true>;
+using Tc256x2f = TcCfg<256, 2, 4, 3, 2048, true>;
+using Tc512x1f = TcCfg<512, 1, 4, 3, 2048, true>;
+using Tc512x2f = TcCfg<512, 2, 4, 3, 2048, true>;
 
 template <template <class> class Fn, class... Args>
-cudaError_t with_tc_cfg(int HS, int G, int group_bytes, Args&&... args) {
+cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, Args&&... args) {
   const bool two = G > 8;
+  if (kv8) {
+    switch (HS) {
+      case 64: return two ? Fn<Tc64x2f>::run(args...) : Fn<Tc64x1f>::run(args...);
+      case 128: return two ? Fn<Tc128x2f>::run(args...) : Fn<Tc128x1f>::run(args...);
+      case 256: return two ? Fn<Tc256x2f>::run(args...) : Fn<Tc256x1f>::run(args...);
+      case 512: return two ? Fn<Tc512x2f>::run(args...) : Fn<Tc512x1f>::run(args...);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (HS) {
     case 64: return two ? Fn<Tc64x2>::run(args...) : Fn<Tc64x1>::run(args...);
     case 128: return two ? Fn<Tc128x2>::run(args...) : Fn<Tc128x1>::run(args...);
@@ -1086,7 +1237,7 @@ int plan_granule(int path, int HS) {
   return 1;
 }
 
-cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas) {
+cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas) {
   if (path == FD_PATH_SIMT) {
     const size_t sm = simt_smem_bytes(G, HS);
     cudaError_t e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1094,11 +1245,11 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, int* ctas) {
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_simt_kernel, kSimtThreads, sm);
   }
-  return with_tc_cfg<OccFn>(HS, G, 2048, ctas);
+  return with_tc_cfg<OccFn>(HS, G, 2048, kv8, ctas);
 }
 
-cudaError_t query_max_cluster(int HS, int G, int* cluster) {
-  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, cluster);
+cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster) {
+  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, cluster);
 }
 
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
@@ -1111,7 +1262,7 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     dim3 grid(a.num_splits, a.NKV, a.B);
     e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, 1, a);
   } else {
-    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a, stream);
+    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a, stream);
   }
   // the split kernel wrote the output itself: one block / cluster per band, or
   // the fused merge by each group's last block

@@ -79,6 +79,12 @@ enum {
   FD_DEVERR_WAIT_TIMEOUT = 1u << 2   /* a pipeline wait gave up; the output is invalid */
 };
 
+/* KV cache element types (fd_plan_t.kv_dtype). */
+enum {
+  FD_KV_BF16 = 0,  /* bf16 K and V: fd_decode_attn, fd_decode_attn_ex, fd_decode_attn_noalloc */
+  FD_KV_E4M3 = 1   /* FP8 E4M3 codes with fp32 scales: fd_decode_attn_fp8, fd_decode_attn_fp8_ex */
+};
+
 /* Kernel families. */
 enum {
   FD_PATH_AUTO = 0,   /* let the plan choose */
@@ -133,7 +139,8 @@ typedef struct {
   int num_sms;             /* SM count the plan assumed */
   int max_cluster;         /* largest cluster the device schedules for this kernel */
   int fused;               /* 1: each group's last split block merges (no merge kernel) */
-  int group_bytes;         /* bytes per bulk-copy group of a tile: 2048, or 4096 (see below) */
+  int group_bytes;         /* bytes per bulk-copy group of a tile: 2048, or 4096 (see below); 1024 for E4M3 */
+  int kv_dtype;            /* FD_KV_BF16 or FD_KV_E4M3: the cache type the plan was made for */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
   size_t workspace_zero_bytes; /* leading workspace bytes that must be zero before first use */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
@@ -158,6 +165,19 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
  */
 int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
                 int num_sms, int ctas_per_sm, int max_cluster, fd_plan_t* plan);
+
+/*
+ * fd_plan_kv / fd_plan_sms_kv: fd_plan / fd_plan_sms for a cache of element
+ * type kv_dtype (FD_KV_BF16 gives the same plan as fd_plan / fd_plan_sms).
+ * An E4M3 plan runs on FD_PATH_TC only, copies 1 KB groups (the same tile
+ * positions as bf16) and bounds a split by the same ~2 MiB of K+V bytes, so
+ * its splits may hold twice the positions.
+ * Errors: FD_ERR_INVALID_ARG (unknown kv_dtype), those of fd_plan / fd_plan_sms.
+ */
+int fd_plan_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
+               int device, int kv_dtype, fd_plan_t* plan);
+int fd_plan_sms_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,
+                   int num_sms, int ctas_per_sm, int max_cluster, int kv_dtype, fd_plan_t* plan);
 
 /*
  * fd_plan_override: force the split count (num_splits >= 1; 0 keeps the
@@ -212,6 +232,44 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
                       const void* v_cache, void* out, const int* lens, int B, int NH,
                       int NKV, int HS, int capacity, int window, float scale,
                       fd_stream_t stream);
+
+/*
+ * fd_decode_attn_fp8 / fd_decode_attn_fp8_ex: the same attention over an FP8
+ * cache. "Hand-Writing Gemma 4 Flash-Decoding + an FP4 Matvec Bonus
+ * (Part 2)": the paragraph on the open problem just before section "What we'd
+ * tell the next person" leaves the long-band MQA latency residual to FP8 KV
+ * storage, which halves the bytes per position; that section adds that FP8
+ * KV needs no special hardware, the values being widened inline where they
+ * are used. Reading taken (the page fixes no scale granularity): one fp32
+ * scale per (sequence, KV head) for K and one for V.
+ *     k8, v8    uint8 [B][NKV][capacity][HS]  E4M3 codes (1 sign, 4 exponent
+ *                                             bits with bias 7, 3 mantissa
+ *                                             bits; no infinity; x111_1111 NaN)
+ *     k_scale   fp32  [B][NKV]   K[b][kvh][slot][d] = E4M3(k8[...]) * k_scale[b][kvh]
+ *     v_scale   fp32  [B][NKV]   the same for V
+ * q, out, out_f32, lens and every other convention are those of
+ * fd_decode_attn / fd_decode_attn_ex; k8 and v8 must be 16-byte aligned and
+ * the scales 4-byte aligned. Arithmetic: every E4M3 value is an fp16 value,
+ * so codes widen to fp16 exactly; q is scaled by a power of two per block
+ * (exact) and rounded to fp16 (exact for bf16 inputs within 2^-37 of the
+ * block's largest |q|); products accumulate in fp32; the softmax weights
+ * enter the P.V product as fp16 (relative error at most 2^-11 per weight);
+ * O is multiplied by the V scale once at the end. fd_decode_attn_fp8_ex needs
+ * an FD_KV_E4M3 plan (fd_plan_kv) and the bf16 entry points an FD_KV_BF16
+ * plan; a plan of the other type is FD_ERR_INVALID_ARG. Workspace: as for
+ * fd_decode_attn / fd_decode_attn_ex (fd_decode_attn_fp8 shares the
+ * library-owned workspaces).
+ * Errors: every FD_ERR_* code.
+ */
+int fd_decode_attn_fp8(const void* q, const void* k8, const void* v8, const float* k_scale,
+                       const float* v_scale, void* out, const int* lens, int B, int NH,
+                       int NKV, int HS, int capacity, int window, float scale,
+                       fd_stream_t stream);
+int fd_decode_attn_fp8_ex(const fd_plan_t* plan, void* workspace, size_t workspace_bytes,
+                          float* out_f32, const void* q, const void* k8, const void* v8,
+                          const float* k_scale, const float* v_scale, void* out,
+                          const int* lens, int B, int NH, int NKV, int HS, int capacity,
+                          int window, float scale, fd_stream_t stream);
 
 /*
  * fd_decode_attn_noalloc: the same computation as fd_decode_attn, for callers

@@ -35,8 +35,8 @@
 //
 // A third computes the same attention over an FP8 (E4M3) cache: the same
 // page's section "What we'd tell the next person" says FP8 KV storage needs
-// no special hardware and is dequantised inline ("storage format is not
-// compute format"). Reading taken: K and V are stored as E4M3 codes with one
+// no special hardware and is dequantised inline: the type a cache is stored
+// in need not be the type the arithmetic runs in. Reading taken: K and V are stored as E4M3 codes with one
 // fp32 scale per (sequence, KV head) for K and one for V; the value of a code
 // is its E4M3 number times that scale. E4M3 (1 sign, 4 exponent bits with
 // bias 7, 3 mantissa bits; exponent field 0 = subnormal; code x111_1111 =

@@ -109,3 +109,44 @@ def oracle_ref(w, q, k, v, lens, rows=None):
         for b, h in rows:
             want[b * w.NH + h] = True
     return oracle.decode(q, k, v, lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale, want=want)
+
+
+def run_fp8(w, q, k8, v8, ks, vs, lens, splits: int = 0, max_len: int = 0, device="cuda",
+            inputs_on_device=False, scale=None, cluster: int = 0, fused: int = -1):
+    """One fd_decode_attn_fp8_ex call over an E4M3 cache (codes k8/v8, scales
+    ks/vs); same result dict as run()."""
+    dev = torch.device(device)
+    if inputs_on_device:
+        qd, kd, vd, ksd, vsd, ld = q, k8, v8, ks, vs, lens.to(dev)
+    else:
+        qd, kd, vd, ksd, vsd, ld = (t.to(dev) for t in (q, k8, v8, ks, vs, lens))
+    plan = fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len, kv_dtype=fd.FD_KV_E4M3)
+    if splits or cluster or fused >= 0:
+        fd.fd_plan_override(plan, splits, 0, cluster, fused)
+    n = w.B * w.NH * w.HS
+    o16 = Guarded(n * 2, dev, fill=0xFF)
+    o32 = Guarded(n * 4, dev, fill=0xFF)
+    ws = Guarded(plan.workspace_bytes, dev, fill=0xFF)
+    if plan.workspace_zero_bytes:
+        ws.body[: plan.workspace_zero_bytes].zero_()
+    fd.fd_get_device_error()
+    fd.fd_decode_attn_fp8_ex(plan, ws.ptr() if plan.workspace_bytes else None, plan.workspace_bytes, o32.ptr(),
+                             qd, kd, vd, ksd, vsd, o16.ptr(), ld, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
+                             w.scale if scale is None else scale)
+    torch.cuda.synchronize()
+    err = fd.fd_get_device_error()
+    counters_zero = bool((ws.body[: plan.workspace_zero_bytes] == 0).all().item()) if plan.workspace_zero_bytes else True
+    return dict(out=o16.view(torch.bfloat16, (w.B, w.NH, w.HS)).cpu(),
+                out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(),
+                plan=plan, deverr=err, counters_zero=counters_zero,
+                canaries=o16.canaries_intact() and o32.canaries_intact() and ws.canaries_intact())
+
+
+def oracle_ref_fp8(w, q, k8, v8, ks, vs, lens, rows=None):
+    want = None
+    if rows is not None:
+        want = np.zeros(w.B * w.NH, dtype=bool)
+        for b, h in rows:
+            want[b * w.NH + h] = True
+    return oracle.decode_fp8(q, k8, v8, ks.cpu().numpy(), vs.cpu().numpy(), lens, w.B, w.NH, w.NKV, w.HS,
+                             w.capacity, w.window, w.scale, want=want)

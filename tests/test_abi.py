@@ -187,3 +187,59 @@ def test_binding_raises_fderror(lib):
     with pytest.raises(fd.FdError) as e:
         fd.fd_plan_sms(1, 16, 8, 96, 64, 0, 0, 152, 2)
     assert e.value.status == fd.FD_ERR_UNSUPPORTED
+
+
+def _plan_kv(w, kv=fd.FD_KV_E4M3, sms=152, ctas=2, max_len=0):
+    return fd.fd_plan_sms_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len, sms, ctas, 8, kv)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_e4m3_plan_matches_bf16_rule_with_half_the_bytes(name, lib):
+    w = WORKLOADS[name]
+    p8, p16 = _plan_kv(w), _plan(w)
+    assert p8.kv_dtype == fd.FD_KV_E4M3 and p16.kv_dtype == fd.FD_KV_BF16
+    assert p8.group_bytes == 1024 and p8.path == fd.FD_PATH_TC
+    # the same SM fill; a split is bounded by the same ~2 MiB of K+V bytes,
+    # which at 2 bytes per position pair is twice the positions
+    chunk8 = -(-p8.max_band // p8.num_splits)
+    assert chunk8 * w.HS * 2 <= (2 << 20) + w.HS * 2
+    assert p8.num_splits <= p16.num_splits
+    # a bf16 plan from fd_plan_sms_kv is fd_plan_sms's plan
+    same = _plan_kv(w, fd.FD_KV_BF16)
+    assert bytes(same) == bytes(p16)
+
+
+def test_e4m3_plan_rejects_the_simt_path_and_unknown_types(lib):
+    w = WORKLOADS["gemma_local_ring"]
+    p = _plan_kv(w)
+    with pytest.raises(fd.FdError) as e:
+        fd.fd_plan_override(p, 0, fd.FD_PATH_SIMT)
+    assert e.value.status == fd.FD_ERR_INVALID_ARG
+    fd.fd_plan_override(p, 9, fd.FD_PATH_TC)  # split count and clusters still move
+    assert p.num_splits == 9 and p.group_bytes == 1024
+    pp = fd.fd_plan_t()
+    assert lib.fd_plan_sms_kv(1, 16, 8, 256, 64, 0, 0, 152, 2, 8, 2, ctypes.byref(pp)) == fd.FD_ERR_INVALID_ARG
+    assert lib.fd_plan_kv(1, 16, 8, 256, 64, 0, 0, 0, 7, ctypes.byref(pp)) == fd.FD_ERR_INVALID_ARG
+
+
+def test_e4m3_argument_errors_before_any_cuda_call(lib):
+    w = WORKLOADS["gemma_local_ring"]
+    p8, p16 = _plan_kv(w), _plan(w)
+    args = (w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
+    A = 1 << 20  # fake, aligned addresses; nothing is dereferenced on these paths
+    ex8, ex16 = lib.fd_decode_attn_fp8_ex, lib.fd_decode_attn_ex
+    ws = p8.workspace_bytes
+    # a plan of the other cache type
+    assert ex8(ctypes.byref(p16), A, p16.workspace_bytes, None, A, A, A, A, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    assert ex16(ctypes.byref(p8), A, ws, None, A, A, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    # missing or misaligned scales
+    assert ex8(ctypes.byref(p8), A, ws, None, A, A, A, None, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    assert ex8(ctypes.byref(p8), A, ws, None, A, A, A, A, None, A, A, *args) == fd.FD_ERR_INVALID_ARG
+    assert ex8(ctypes.byref(p8), A, ws, None, A, A, A, A + 2, A, A, A, *args) == fd.FD_ERR_ALIGNMENT
+    # misaligned codes, short workspace
+    assert ex8(ctypes.byref(p8), A, ws, None, A, A + 8, A, A, A, A, A, *args) == fd.FD_ERR_ALIGNMENT
+    assert ex8(ctypes.byref(p8), A, ws - 1, None, A, A, A, A, A, A, A, *args) == fd.FD_ERR_WORKSPACE
+    # the auto entry point checks shapes and scales before touching the device
+    bad = (1, 16, 8, 96, 64, 0, 0.0, None)
+    assert lib.fd_decode_attn_fp8(A, A, A, A, A, A, A, *bad) == fd.FD_ERR_UNSUPPORTED
+    assert lib.fd_decode_attn_fp8(A, A, A, None, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
