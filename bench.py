@@ -155,27 +155,46 @@ def layers_for(w, live, cap_layers=256):
 
 
 class Step:
-    """L layers of one geometry resident on the device."""
+    """L layers of one geometry resident on the device; kv = "bf16" or "e4m3"
+    (E4M3 codes with per-(sequence, KV head) scales: half the live bytes)."""
 
-    def __init__(self, w, layers, device, seed_base=0):
-        from decode_attention_04_gb300.inputs import draw_lens, make_inputs
+    def __init__(self, w, layers, device, seed_base=0, kv="bf16"):
+        from decode_attention_04_gb300.inputs import draw_lens, make_inputs, make_inputs_fp8
 
         self.w = w
         self.L = layers
+        self.kv = kv
         self.lens_h = draw_lens(w)
-        self.q, self.k, self.v = [], [], []
+        self.q, self.k, self.v, self.ks, self.vs = [], [], [], [], []
         for i in range(layers):
-            q, k, v, _ = make_inputs(w, device=device, seed=w.seed * 1000 + seed_base + i, lens=self.lens_h)
+            seed = w.seed * 1000 + seed_base + i
+            if kv == "e4m3":
+                q, k, v, ks, vs, _ = make_inputs_fp8(w, device=device, seed=seed, lens=self.lens_h)
+                self.ks.append(ks)
+                self.vs.append(vs)
+            else:
+                q, k, v, _ = make_inputs(w, device=device, seed=seed, lens=self.lens_h)
             self.q.append(q)
             self.k.append(k)
             self.v.append(v)
         self.lens = self.lens_h.to(device)
         self.out = [torch.empty_like(x) for x in self.q]
-        self.live = live_band_bytes(w, self.lens_h)
+        self.live = live_band_bytes(w, self.lens_h) // (2 if kv == "e4m3" else 1)
+
+    def plan(self):
+        import decode_attention_04_gb300 as fd
+        w = self.w
+        kv = fd.FD_KV_E4M3 if self.kv == "e4m3" else fd.FD_KV_BF16
+        return fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, kv_dtype=kv)
 
     def run(self, stream=None):
         import decode_attention_04_gb300 as fd
         w = self.w
+        if self.kv == "e4m3":
+            for i in range(self.L):
+                fd.fd_decode_attn_fp8(self.q[i], self.k[i], self.v[i], self.ks[i], self.vs[i], self.out[i],
+                                      self.lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale, stream)
+            return
         for i in range(self.L):
             fd.fd_decode_attn(self.q[i], self.k[i], self.v[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
                               w.capacity, w.window, w.scale, stream)
@@ -261,17 +280,15 @@ def cpu_baseline(w, step: Step, budget_s: float = 10.0):
                       f"FP64, {cores} threads, {t_used:.2f} s"}
 
 
-def run_geometry(w, steps, warmup, stream, device, peak):
-    import decode_attention_04_gb300 as fd
-
+def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
     from decode_attention_04_gb300.inputs import draw_lens
     lens = draw_lens(w)
     live = live_band_bytes(w, lens)
     L = layers_for(w, live)
-    st = Step(w, L, device)
+    st = Step(w, L, device, kv=kv)
     ms, _ = time_graph(st, steps, warmup, stream)
     t = statistics.median(ms)
-    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    plan = st.plan()
     gbs = st.live * L / (t * 1e-3) / 1e9
     res = {"us_per_layer": t * 1e3 / L, "us_per_layer_min": min(ms) * 1e3 / L, "live_GBps": gbs,
            "frac_of_peak": gbs / peak, "layers": L, "live_bytes_per_layer": st.live,
@@ -292,6 +309,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling mode: N plain fd_decode_attn calls on one layer of --workload, then exit")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
+                    help="cache type of --profile-calls (the timed step and its line are bf16)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -304,7 +323,7 @@ def main():
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
     if args.profile_calls:
-        return profile_calls(w, args.profile_calls)
+        return profile_calls(w, args.profile_calls, args.kv)
 
     import decode_attention_04_gb300 as fd
     from decode_attention_04_gb300 import build as libbuild
@@ -358,13 +377,15 @@ def main():
     live = step.live
     del graph
     clocks = clk.summary()
-    geoms = None
+    geoms = geoms8 = None
     if not args.no_geometries:
         del step
         torch.cuda.empty_cache()
-        geoms = {}
+        geoms, geoms8 = {}, {}
         for name, gw in WORKLOADS.items():
             geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak)
+        for name, gw in WORKLOADS.items():
+            geoms8[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak, kv="e4m3")
 
     traffic = None
     tf = ROOT / "profiles" / "traffic.txt"
@@ -415,6 +436,7 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "geometries": geoms,
+        "geometries_e4m3": geoms8 if not args.no_geometries else None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -423,16 +445,16 @@ def main():
     return 0
 
 
-def profile_calls(w, n):
+def profile_calls(w, n, kv="bf16"):
     """N plain calls on one layer (for ncu launch lists and captures)."""
     from decode_attention_04_gb300 import build as libbuild
     libbuild.build()
     device = torch.device("cuda", 0)
-    st = Step(w, 1, device)
+    st = Step(w, 1, device, kv=kv)
     for _ in range(n):
         st.run()
     torch.cuda.synchronize()
-    print(json.dumps({"profile_calls": n, "workload": w.name, "live_bytes": st.live}), flush=True)
+    print(json.dumps({"profile_calls": n, "workload": w.name, "kv": kv, "live_bytes": st.live}), flush=True)
     return 0
 
 

@@ -215,6 +215,10 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                               uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -378,9 +382,16 @@ size_t simt_smem_bytes(int G, int HS) {
 // the softmax does not depend on the order of positions.
 //
 // E4M3 caches (KV8): the ring holds the codes in 1 KB groups (the same tile
-// positions as the bf16 tile, half the bytes); the consumers widen each
-// arrived stage into one fp16 tile laid out as the bf16 tile is, and release
-// the stage at once, so the copies of later tiles overlap the MMAs.
+// positions as the bf16 tile, half the bytes), and the consumers build fp16
+// MMA fragments from it in registers. The order of the k index of an MMA is
+// free as long as both operands use the same one, so for S^T = K Q^T a
+// thread's four k slots are four consecutive head dims (one 32-bit load per
+// K row); for O^T = V^T P^T the k slots are MMA rows as usual and a
+// thread's 32-bit load holds four consecutive dims of one position, which
+// byte permutes split into the rows of two MMAs: accumulator row grp of
+// MMA 2c holds dim 32c + 4 grp, row grp + 8 dim 32c + 4 grp + 1, and MMA
+// 2c + 1 the dims + 2 and + 3. With the 16-byte group padding both load
+// patterns are free of bank conflicts.
 template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048, bool KV8_ = false>
 struct TcCfg {
   static constexpr bool KV8 = KV8_;
@@ -403,8 +414,8 @@ struct TcCfg {
   static constexpr int TPR = CTHREADS / NP;  // softmax threads per query row
   static constexpr int PPT = T / TPR;        // positions per softmax thread
   static constexpr size_t STAGE_BYTES = static_cast<size_t>(NG) * GP;
-  // compute-layout tiles held: the copy ring itself (bf16), or one widened tile (KV8)
-  static constexpr int NBUF = KV8 ? 1 : NSTAGE;
+  // bf16 tiles held: the copy ring itself, or none (KV8 reads its own ring)
+  static constexpr int NBUF = KV8 ? 0 : NSTAGE;
   static constexpr int ROWB8 = HS;                // bytes of one E4M3 cache row
   static constexpr int GP8 = R * ROWB8 + 16;      // E4M3 group pitch, bytes
   static constexpr size_t STAGE8_BYTES = KV8 ? static_cast<size_t>(NG) * GP8 : 0;
@@ -424,6 +435,12 @@ struct TcCfg {
   __device__ static __forceinline__ int off_of(int m) { return (m % NG) * GP + (m / NG) * ROWB; }
   // byte offset of tile position j in a stage
   __device__ static __forceinline__ int off_pos(int j) { return (j / R) * GP + (j % R) * ROWB; }
+  // byte offset of MMA row m in an E4M3 stage
+  __device__ static __forceinline__ int off8_of(int m) { return (m % NG) * GP8 + (m / NG) * ROWB8; }
+  // head dim (within the warp's slice) of accumulator row grp (+ 8 when hi) of dim-MMA mt
+  __device__ static __forceinline__ int dim_of(int mt, int grp, int hi) {
+    return KV8 ? 32 * (mt >> 1) + 4 * grp + 2 * (mt & 1) + hi : mt * 16 + grp + hi * 8;
+  }
   // smallest tile position among MMA rows [16 mt, 16 mt + 16)
   __device__ static __forceinline__ int min_pos(int mt) { return pos_of(16 * mt); }
 
@@ -437,6 +454,7 @@ struct TcCfg {
   // once the last tile is consumed), weights in the score buffer
   static_assert(static_cast<size_t>(NP) * HS * 4 <= OFF_S, "O must fit the tile buffers");
   static_assert(!KV8 || (GP8 % 16 == 0 && R * ROWB8 == 1024), "E4M3 groups are 1 KB, 16-byte aligned");
+  static_assert(!KV8 || DW % 32 == 0, "E4M3 fragments take head dims 32 at a time");
   static_assert(NP * 16 + 2 * NP <= NWC * NP * SP, "cluster weights must fit the score buffer");
   static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
@@ -559,7 +577,9 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   // -------------------------------------------------------------- consumers
 
   // Q^T as MMA B fragments for this warp's dims: b0 = (dims 2t4..2t4+1, row grp),
-  // b1 = (dims 8+2t4.., row grp) of each 16-dim step.
+  // b1 = (dims 8+2t4.., row grp) of each 16-dim step; for KV8 (k slots =
+  // consecutive dims) b0 = dims 4t4..4t4+1, b1 = dims 4t4+2..4t4+3.
+  constexpr int kQLo = C::KV8 ? 4 : 2, kQHi = C::KV8 ? 2 : 8;
   uint32_t qf[C::KD][C::NT][2];
 #pragma unroll
   for (int ks = 0; ks < C::KD; ++ks)
@@ -568,9 +588,9 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       const int r = nt * 8 + grp;
       uint32_t x0 = 0, x1 = 0;
       if (r < G) {
-        const uint16_t* qr = a.q + (static_cast<size_t>(b) * a.NH + hbase + r) * C::HS + dbase + ks * 16 + 2 * t4;
+        const uint16_t* qr = a.q + (static_cast<size_t>(b) * a.NH + hbase + r) * C::HS + dbase + ks * 16 + kQLo * t4;
         x0 = *reinterpret_cast<const uint32_t*>(qr);
-        x1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+        x1 = *reinterpret_cast<const uint32_t*>(qr + kQHi);
       }
       qf[ks][nt][0] = x0;
       qf[ks][nt][1] = x1;
@@ -623,34 +643,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     const int st = i % C::NSTAGE;
     mbar_wait(full0 + 8 * st, (i / C::NSTAGE) & 1, failed);
     const int nv = min(C::T, n - i * C::T);  // valid tile positions: [0, nv)
-    const int buf = C::KV8 ? 0 : st;
-    const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(buf) * C::STAGE_BYTES;
-    unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(buf) * C::STAGE_BYTES;
-    if constexpr (C::KV8) {
-      // E4M3 stage -> fp16 tile, 8 codes per step (positions >= nv become
-      // zeros, so a 0-weight position contributes exactly 0); then the stage
-      // goes back to the producers.
-      if (i > 0) named_bar_sync(1, C::CTHREADS);  // every consumer is done with the previous tile
-      const unsigned char* fK = smem + C::OFF_K8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
-      const unsigned char* fV = smem + C::OFF_V8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
-      constexpr int CH = C::HS / 8;  // 8-code chunks per row
-      for (int w8 = tid; w8 < 2 * C::T * CH; w8 += C::CTHREADS) {
-        const int tensor = w8 / (C::T * CH), rem = w8 % (C::T * CH);
-        const int j = rem / CH, c = rem % CH;
-        uint4 h = make_uint4(0, 0, 0, 0);
-        if (j < nv) {
-          const uint2 codes = *reinterpret_cast<const uint2*>((tensor ? fV : fK) + (j / C::R) * C::GP8 +
-                                                              (j % C::R) * C::ROWB8 + c * 8);
-          h = make_uint4(e4m3x2_to_f16x2(codes.x & 0xffffu), e4m3x2_to_f16x2(codes.x >> 16),
-                         e4m3x2_to_f16x2(codes.y & 0xffffu), e4m3x2_to_f16x2(codes.y >> 16));
-        }
-        unsigned char* dstp = (tensor ? tV : const_cast<unsigned char*>(tK)) + C::off_pos(j) + c * 16;
-        *reinterpret_cast<uint4*>(dstp) = h;
-      }
-      named_bar_sync(1, C::CTHREADS);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * st);
-    }
+    const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES;
+    unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
+    // E4M3 stage (KV8)
+    [[maybe_unused]] const unsigned char* fK = smem + C::OFF_K8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
+    [[maybe_unused]] const unsigned char* fV = smem + C::OFF_V8 + static_cast<size_t>(st) * C::STAGE8_BYTES;
 
     // ---- scores: S^T[m][row] partial over this warp's dims (m = MMA row order)
     float* myS = sS + static_cast<size_t>(warp) * C::NP * C::SP;
@@ -662,18 +659,31 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        if constexpr (C::KV8) {
+          // rows mt*16 + grp and + 8; k slots 2t4, 2t4+1 / 2t4+8, 2t4+9 = dims 4t4 .. 4t4+3
+          const unsigned char* k0 = fK + C::off8_of(mt * 16 + grp) + dbase + 4 * t4;
 #pragma unroll
-        for (int ks = 0; ks < C::KD; ++ks) {
-          // matrices: (rows 0-7, d 0-7), (rows 8-15, d 0-7), (rows 0-7, d 8-15), (rows 8-15, d 8-15)
-          const int m = mt * 16 + lrow + (lmat & 1) * 8;
-          const int dcol = dbase + ks * 16 + (lmat >> 1) * 8;
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(smem_u32(tK + C::off_of(m) + dcol * 2), a0, a1, a2, a3);
+          for (int ks = 0; ks < C::KD; ++ks) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(k0 + ks * 16);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(k0 + C::ROWB8 + ks * 16);
+            const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0 & 0xffffu));
+            const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16));
+            const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1 & 0xffffu));
+            const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(w1 >> 16));
 #pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) {
-            if constexpr (C::KV8)
+            for (int nt = 0; nt < C::NT; ++nt)
               mma_f16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
-            else
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < C::KD; ++ks) {
+            // matrices: (rows 0-7, d 0-7), (rows 8-15, d 0-7), (rows 0-7, d 8-15), (rows 8-15, d 8-15)
+            const int m = mt * 16 + lrow + (lmat & 1) * 8;
+            const int dcol = dbase + ks * 16 + (lmat >> 1) * 8;
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(smem_u32(tK + C::off_of(m) + dcol * 2), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt)
               mma_bf16_16816(acc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
           }
         }
@@ -752,7 +762,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
     named_bar_sync(1, C::CTHREADS);
 
-    // ---- O^T[dim][row] = alpha * O^T + V^T P^T  (P split into bf16 hi + lo)
+    // ---- O^T[dim][row] = alpha * O^T + V^T P^T  (P split into bf16 hi + lo; one fp16 P for KV8)
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt) {
       const float al0 = sAlpha[nt * 8 + 2 * t4], al1 = sAlpha[nt * 8 + 2 * t4 + 1];
@@ -772,20 +782,57 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         for (int nt = 0; nt < C::NT; ++nt) {
           // matrices: (hi, pos 0-7), (hi, pos 8-15), (lo, pos 0-7), (lo, pos 8-15); rows = query rows
           const uint16_t* pa = sP + ((lmat >> 1) * C::NP + nt * 8 + lrow) * C::PPITCH + kp * 16 + (lmat & 1) * 8;
-          ldsm_x4(smem_u32(pa), pb[nt][0], pb[nt][1], pb[nt][2], pb[nt][3]);
+          if constexpr (C::KV8) {
+            ldsm_x2(smem_u32(pa), pb[nt][0], pb[nt][1]);  // fp16 P: no lo half
+          } else {
+            ldsm_x4(smem_u32(pa), pb[nt][0], pb[nt][1], pb[nt][2], pb[nt][3]);
+          }
         }
+        if constexpr (C::KV8) {
+          // k slots 2t4, 2t4+1, 2t4+8, 2t4+9 are MMA rows m0, m0+1, m0+8, m0+9;
+          // a load of a row past the tile's valid positions reads 0 instead
+          // (its P is 0, and stale codes may be NaN).
+          const int m0 = kp * 16 + 2 * t4;
+          const int mr[4] = {m0, m0 + 1, m0 + 8, m0 + 9};
+          const unsigned char* vr[4];
+          bool ok[4];
 #pragma unroll
-        for (int mt = 0; mt < C::KD; ++mt) {
-          // V^T fragments: matrices (d 0-7, rows 0-7), (d 8-15, rows 0-7), (d 0-7, rows 8-15), (d 8-15, rows 8-15)
-          const int m = kp * 16 + lrow + (lmat >> 1) * 8;
-          const int dcol = dbase + mt * 16 + (lmat & 1) * 8;
-          uint32_t v0, v1, v2, v3;
-          ldsm_x4_trans(smem_u32(tV + C::off_of(m) + dcol * 2), v0, v1, v2, v3);
+          for (int i = 0; i < 4; ++i) {
+            vr[i] = fV + C::off8_of(mr[i]) + dbase + 4 * grp;
+            ok[i] = C::pos_of(mr[i]) < nv;
+          }
 #pragma unroll
-          for (int nt = 0; nt < C::NT; ++nt) {
-            if constexpr (C::KV8) {
-              mma_f16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
-            } else {
+          for (int c = 0; c < C::DW / 32; ++c) {
+            uint32_t L[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) L[i] = ok[i] ? *reinterpret_cast<const uint32_t*>(vr[i] + 32 * c) : 0u;
+            // byte j of L[i] = dim 4 grp + j of row mr[i]; pair rows (0,1) and (2,3) per dim
+            const uint32_t x01 = __byte_perm(L[0], L[1], 0x5140), x23 = __byte_perm(L[2], L[3], 0x5140);
+            const uint32_t y01 = __byte_perm(L[0], L[1], 0x7362), y23 = __byte_perm(L[2], L[3], 0x7362);
+            const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xffffu));  // dim +0
+            const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16));      // dim +1
+            const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 & 0xffffu));
+            const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x23 >> 16));
+            const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y01 & 0xffffu));  // dim +2
+            const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y01 >> 16));      // dim +3
+            const uint32_t b2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y23 & 0xffffu));
+            const uint32_t b3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y23 >> 16));
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
+              mma_f16_16816(o[2 * c][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+              mma_f16_16816(o[2 * c + 1][nt], b0, b1, b2, b3, pb[nt][0], pb[nt][1]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int mt = 0; mt < C::KD; ++mt) {
+            // V^T fragments: matrices (d 0-7, rows 0-7), (d 8-15, rows 0-7), (d 0-7, rows 8-15), (d 8-15, rows 8-15)
+            const int m = kp * 16 + lrow + (lmat >> 1) * 8;
+            const int dcol = dbase + mt * 16 + (lmat & 1) * 8;
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_trans(smem_u32(tV + C::off_of(m) + dcol * 2), v0, v1, v2, v3);
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
               mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][0], pb[nt][1]);
               mma_bf16_16816(o[mt][nt], v0, v1, v2, v3, pb[nt][2], pb[nt][3]);
             }
@@ -793,10 +840,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         }
       }
     }
-    if constexpr (!C::KV8) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * st);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * st);
   }
 
     if constexpr (C::KV8) {  // O in dequantised units: times this head's V scale
@@ -827,7 +872,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         for (int e = 0; e < 4; ++e) {
           const int r = nt * 8 + 2 * t4 + (e & 1);
           if (r >= G) continue;
-          const int d = dbase + mt * 16 + grp + (e >> 1) * 8;
+          const int d = dbase + C::dim_of(mt, grp, e >> 1);
           const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
           if (direct) {
             const float val = o[mt][nt][e] / sL[r];
@@ -927,7 +972,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = nt * 8 + 2 * t4 + (e & 1);
-          if (r < G) sO[r * C::HS + dbase + mt * 16 + grp + (e >> 1) * 8] = o[mt][nt][e];
+          if (r < G) sO[r * C::HS + dbase + C::dim_of(mt, grp, e >> 1)] = o[mt][nt][e];
         }
   }
   cluster_sync_all();
@@ -1138,10 +1183,10 @@ using Tc256x2 = TcCfg<256, 2, 4, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;
 using Tc512x2 = TcCfg<512, 2, 4, 3>;
 using Tc512x2w = TcCfg<512, 2, 4, 3, 4096>;  // one block per SM, 4 KB copies
-// E4M3 caches: 1 KB copy groups (the same tile positions as the bf16 tiles),
-// a three-stage E4M3 ring and one fp16 tile.
-using Tc64x1f = TcCfg<64, 1, 4, 3, 2048, true>;
-using Tc64x2f = TcCfg<64, 2, 4, 3, 2048, true>;
+// E4M3 caches: 1 KB copy groups (the same tile positions as the bf16 tiles)
+// in a three-stage ring that the MMAs read directly.
+using Tc64x1f = TcCfg<64, 1, 2, 3, 2048, true>;  // two consumer warps: 32 dims each
+using Tc64x2f = TcCfg<64, 2, 2, 3, 2048, true>;
 using Tc128x1f = TcCfg<128, 1, 4, 3, 2048, true>;
 using Tc128x2f = TcCfg<128, 2, 4, 3, 2048, true>;
 using Tc256x1f = TcCfg<256, 1, 4, 3, 2048, true>;
