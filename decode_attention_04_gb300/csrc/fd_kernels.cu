@@ -766,6 +766,9 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt) {
       const float al0 = sAlpha[nt * 8 + 2 * t4], al1 = sAlpha[nt * 8 + 2 * t4 + 1];
+      // once the running maxima settle, alpha is exactly 1 for every row: skip
+      // the multiplies (x * 1 == x, so the result is the same either way)
+      if (!__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) continue;
 #pragma unroll
       for (int mt = 0; mt < C::KD; ++mt) {
         o[mt][nt][0] *= al0;
@@ -1189,10 +1192,10 @@ using Tc64x1f = TcCfg<64, 1, 2, 3, 2048, true>;  // two consumer warps: 32 dims 
 using Tc64x2f = TcCfg<64, 2, 2, 3, 2048, true>;
 using Tc128x1f = TcCfg<128, 1, 4, 3, 2048, true>;
 using Tc128x2f = TcCfg<128, 2, 4, 3, 2048, true>;
-using Tc256x1f = TcCfg<256, 1, 4, 3, 2048, true>;
-using Tc256x2f = TcCfg<256, 2, 4, 3, 2048, true>;
-using Tc512x1f = TcCfg<512, 1, 4, 3, 2048, true>;
-using Tc512x2f = TcCfg<512, 2, 4, 3, 2048, true>;
+using Tc256x1f = TcCfg<256, 1, 8, 3, 2048, true>;  // eight consumer warps: shorter per-warp chains
+using Tc256x2f = TcCfg<256, 2, 8, 3, 2048, true>;
+using Tc512x1f = TcCfg<512, 1, 4, 3, 2048, true>;  // a 16-position tile has 8 x 16 softmax slots
+using Tc512x2f = TcCfg<512, 2, 8, 3, 2048, true>;
 
 template <template <class> class Fn, class... Args>
 cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, Args&&... args) {
