@@ -54,6 +54,7 @@ class fd_plan_t(ctypes.Structure):
         ("fused", ctypes.c_int),
         ("group_bytes", ctypes.c_int),
         ("kv_dtype", ctypes.c_int),
+        ("consumer_warps", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("workspace_zero_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),

@@ -75,16 +75,39 @@ int fused_rule(const fd_plan_t& p) {
 
 // 4 KB copy groups (a tile that needs the whole SM) only for the head-dim-512,
 // 16-row tile, and only when the grid fits one wave at one block per SM.
+// E4M3 groups: 2 KB (1 KB for head dim 256, whose small sliding bands want
+// short tiles).
 int group_rule(const fd_plan_t& p) {
-  if (p.kv_dtype == FD_KV_E4M3) return 1024;  // E4M3 tiles: the same positions, half the bytes
   const long long G = p.NH / p.NKV;
   const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
+  if (p.kv_dtype == FD_KV_E4M3) return p.HS == 256 ? 1024 : 2048;
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
+}
+
+// Consumer warps of the tensor-core tile: fixed per (cache type, head dim,
+// G <= 8 or not), except the E4M3 head-dim-512, 16-row tile: eight warps when
+// the grid is one block per SM, four when blocks share SMs. 0 on the SIMT path.
+bool warps_choice_open(const fd_plan_t& p) {
+  return p.path == FD_PATH_TC && p.kv_dtype == FD_KV_E4M3 && p.HS == 512 && p.NH / p.NKV > 8;
+}
+
+int warps_rule(const fd_plan_t& p) {
+  if (p.path != FD_PATH_TC) return 0;
+  const bool two = p.NH / p.NKV > 8;
+  if (p.kv_dtype == FD_KV_E4M3) {
+    if (p.HS == 64) return 2;
+    if (p.HS == 128) return 4;
+    if (p.HS == 256) return 8;
+    const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
+    return two && blocks <= p.num_sms ? 8 : 4;
+  }
+  return (p.HS == 256 || (p.HS == 512 && two)) ? 8 : 4;
 }
 
 void finish_plan(fd_plan_t* p, int fused = -1) {
   p->fused = fused < 0 ? fused_rule(*p) : (fused && fused_rule_allowed(*p) ? 1 : 0);
   p->group_bytes = group_rule(*p);
+  p->consumer_warps = warps_rule(*p);
   p->workspace_bytes = ws_total(*p);
   p->workspace_zero_bytes = ws_counter_bytes(*p);
 }
@@ -273,6 +296,7 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.ws_ml = need ? reinterpret_cast<float*>(ws + ws_counter_bytes(plan) + ws_o_bytes(plan)) : nullptr;
   a.fused = plan.fused;
   a.group_bytes = plan.group_bytes;
+  a.consumer_warps = plan.consumer_warps;
   a.B = plan.B;
   a.NH = plan.NH;
   a.NKV = plan.NKV;
@@ -370,7 +394,10 @@ int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int 
       !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
       (plan->fused && !fused_rule_allowed(*plan)))
     return FD_ERR_INVALID_ARG;
-  if (kv_dtype == FD_KV_E4M3) return plan->group_bytes == 1024 ? FD_OK : FD_ERR_INVALID_ARG;
+  if (plan->consumer_warps != warps_rule(*plan) &&
+      !(warps_choice_open(*plan) && (plan->consumer_warps == 4 || plan->consumer_warps == 8)))
+    return FD_ERR_INVALID_ARG;
+  if (kv_dtype == FD_KV_E4M3) return plan->group_bytes == group_rule(*plan) ? FD_OK : FD_ERR_INVALID_ARG;
   if ((plan->group_bytes != 2048 && plan->group_bytes != 4096) ||
       (plan->group_bytes == 4096 && group_rule(*plan) != 4096 &&
        !(plan->HS == 512 && plan->NH / plan->NKV > 8 && plan->path == FD_PATH_TC)))

@@ -23,6 +23,7 @@ struct LaunchArgs {
   unsigned int* counters;   // [B][NKV] finished-split counters (fused merge), zero between calls
   int fused;                // 1: the last split block of each (b, kvh) merges; no merge kernel
   int group_bytes;          // bytes per bulk-copy group of the tile (2048, or 4096 for the wide MQA tile)
+  int consumer_warps;       // consumer warps of the split tile (the plan's choice)
   int kv8;                  // 1: the cache is E4M3 codes (k8/v8) with per-(b, kvh) scales
   const uint8_t* k8;        // E4M3 [B][NKV][capacity][HS]  (kv8 only)
   const uint8_t* v8;        // E4M3 [B][NKV][capacity][HS]  (kv8 only)

@@ -453,7 +453,8 @@ struct TcCfg {
   // cluster reduction: O parked in the tile buffers (all of [0, OFF_S) is idle
   // once the last tile is consumed), weights in the score buffer
   static_assert(static_cast<size_t>(NP) * HS * 4 <= OFF_S, "O must fit the tile buffers");
-  static_assert(!KV8 || (GP8 % 16 == 0 && R * ROWB8 == 1024), "E4M3 groups are 1 KB, 16-byte aligned");
+  static_assert(!KV8 || (GP8 % 16 == 0 && (R * ROWB8 == 1024 || R * ROWB8 == 2048)),
+                "E4M3 groups are 1 or 2 KB, 16-byte aligned");
   static_assert(!KV8 || DW % 32 == 0, "E4M3 fragments take head dims 32 at a time");
   static_assert(NP * 16 + 2 * NP <= NWC * NP * SP, "cluster weights must fit the score buffer");
   static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
@@ -1173,39 +1174,48 @@ cudaError_t occupancy_tc(int* ctas) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
 }
 
-// Tile configurations: 8 groups of 2 KB per tensor per stage (about 33 KB of
-// K+V), three stages, two blocks per SM; G <= 8 or G <= 16 query rows per
-// group. The head-dim-512, 16-row tile (the MQA geometry, planned with one
-// block per SM) uses 4 KB groups: 66 KB stages, ~204 KB of shared memory.
+// Tile configurations (measured on GB300, per head dim): 8 groups of 2 KB per
+// tensor per stage (about 33 KB of K+V), three stages, two blocks per SM;
+// G <= 8 or G <= 16 query rows per group. Head dims 256 and 512 use eight
+// consumer warps (shorter per-warp dependency chains; the one-block-per-SM
+// MQA grids gained most). The head-dim-512, 16-row tile planned with one block
+// per SM uses 4 KB groups: 66 KB stages, ~218 KB of shared memory.
 using Tc64x1 = TcCfg<64, 1, 4, 3>;
 using Tc64x2 = TcCfg<64, 2, 4, 3>;
 using Tc128x1 = TcCfg<128, 1, 4, 3>;
 using Tc128x2 = TcCfg<128, 2, 4, 3>;
-using Tc256x1 = TcCfg<256, 1, 4, 3>;
-using Tc256x2 = TcCfg<256, 2, 4, 3>;
-using Tc512x1 = TcCfg<512, 1, 4, 3>;
-using Tc512x2 = TcCfg<512, 2, 4, 3>;
-using Tc512x2w = TcCfg<512, 2, 4, 3, 4096>;  // one block per SM, 4 KB copies
-// E4M3 caches: 1 KB copy groups (the same tile positions as the bf16 tiles)
-// in a three-stage ring that the MMAs read directly.
-using Tc64x1f = TcCfg<64, 1, 2, 3, 2048, true>;  // two consumer warps: 32 dims each
-using Tc64x2f = TcCfg<64, 2, 2, 3, 2048, true>;
-using Tc128x1f = TcCfg<128, 1, 4, 3, 2048, true>;
-using Tc128x2f = TcCfg<128, 2, 4, 3, 2048, true>;
-using Tc256x1f = TcCfg<256, 1, 8, 3, 2048, true>;  // eight consumer warps: shorter per-warp chains
-using Tc256x2f = TcCfg<256, 2, 8, 3, 2048, true>;
-using Tc512x1f = TcCfg<512, 1, 4, 3, 2048, true>;  // a 16-position tile has 8 x 16 softmax slots
-using Tc512x2f = TcCfg<512, 2, 8, 3, 2048, true>;
+using Tc256x1 = TcCfg<256, 1, 8, 3>;
+using Tc256x2 = TcCfg<256, 2, 8, 3>;
+using Tc512x1 = TcCfg<512, 1, 4, 3>;  // a 16-position tile has 8 x 16 softmax slots
+using Tc512x2 = TcCfg<512, 2, 8, 3>;
+using Tc512x2w = TcCfg<512, 2, 8, 3, 4096>;  // one block per SM, 4 KB copies
+// E4M3 caches: a block's copy rate is set by the number of bulk copies it
+// issues, so 2 KB E4M3 groups (the positions of a 4 KB bf16 group) in a
+// two-stage ring, except head dim 256 (small sliding bands), where 1 KB groups
+// in four stages keep a split near one tile. The head-dim-512, 16-row tile
+// takes eight consumer warps when the grid is one block per SM and four
+// otherwise (two blocks per SM share the issue slots).
+using Tc64x1f = TcCfg<64, 1, 2, 2, 4096, true>;  // two consumer warps: 32 dims each
+using Tc64x2f = TcCfg<64, 2, 2, 2, 4096, true>;
+using Tc128x1f = TcCfg<128, 1, 4, 2, 4096, true>;
+using Tc128x2f = TcCfg<128, 2, 4, 2, 4096, true>;
+using Tc256x1f = TcCfg<256, 1, 8, 4, 2048, true>;
+using Tc256x2f = TcCfg<256, 2, 8, 4, 2048, true>;
+using Tc512x1f = TcCfg<512, 1, 4, 2, 4096, true>;
+using Tc512x2f = TcCfg<512, 2, 4, 2, 4096, true>;
+using Tc512x2f8 = TcCfg<512, 2, 8, 2, 4096, true>;  // one block per SM
 
 template <template <class> class Fn, class... Args>
-cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, Args&&... args) {
+cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, int warps, Args&&... args) {
   const bool two = G > 8;
   if (kv8) {
     switch (HS) {
       case 64: return two ? Fn<Tc64x2f>::run(args...) : Fn<Tc64x1f>::run(args...);
       case 128: return two ? Fn<Tc128x2f>::run(args...) : Fn<Tc128x1f>::run(args...);
       case 256: return two ? Fn<Tc256x2f>::run(args...) : Fn<Tc256x1f>::run(args...);
-      case 512: return two ? Fn<Tc512x2f>::run(args...) : Fn<Tc512x1f>::run(args...);
+      case 512:
+        if (!two) return Fn<Tc512x1f>::run(args...);
+        return warps == 8 ? Fn<Tc512x2f8>::run(args...) : Fn<Tc512x2f>::run(args...);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1293,11 +1303,11 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas) {
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_simt_kernel, kSimtThreads, sm);
   }
-  return with_tc_cfg<OccFn>(HS, G, 2048, kv8, ctas);
+  return with_tc_cfg<OccFn>(HS, G, 2048, kv8, 0, ctas);
 }
 
 cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster) {
-  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, cluster);
+  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, 0, cluster);
 }
 
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
@@ -1310,7 +1320,7 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     dim3 grid(a.num_splits, a.NKV, a.B);
     e = launch_pdl(split_simt_kernel, grid, dim3(kSimtThreads), sm, stream, 1, a);
   } else {
-    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a, stream);
+    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, a, stream);
   }
   // the split kernel wrote the output itself: one block / cluster per band, or
   // the fused merge by each group's last block

@@ -139,8 +139,9 @@ typedef struct {
   int num_sms;             /* SM count the plan assumed */
   int max_cluster;         /* largest cluster the device schedules for this kernel */
   int fused;               /* 1: each group's last split block merges (no merge kernel) */
-  int group_bytes;         /* bytes per bulk-copy group of a tile: 2048, or 4096 (see below); 1024 for E4M3 */
+  int group_bytes;         /* bytes per bulk-copy group of a tile: 2048 or 4096 (bf16); 2048 or 1024 (E4M3) */
   int kv_dtype;            /* FD_KV_BF16 or FD_KV_E4M3: the cache type the plan was made for */
+  int consumer_warps;      /* MMA warps per split block (2, 4 or 8; 0 on the SIMT path) */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
   size_t workspace_zero_bytes; /* leading workspace bytes that must be zero before first use */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
@@ -169,9 +170,11 @@ int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int ma
 /*
  * fd_plan_kv / fd_plan_sms_kv: fd_plan / fd_plan_sms for a cache of element
  * type kv_dtype (FD_KV_BF16 gives the same plan as fd_plan / fd_plan_sms).
- * An E4M3 plan runs on FD_PATH_TC only, copies 1 KB groups (the same tile
- * positions as bf16) and bounds a split by the same ~2 MiB of K+V bytes, so
- * its splits may hold twice the positions.
+ * An E4M3 plan runs on FD_PATH_TC only and bounds a split by the same ~2 MiB
+ * of K+V bytes, so its splits may hold twice the positions. Its copy groups
+ * are 2 KB (1 KB for head dim 256) and its head-dim-512, 16-row tile uses
+ * eight consumer warps when the grid is one block per SM, four otherwise
+ * (measured on GB300: copy count per block and issue slots per SM).
  * Errors: FD_ERR_INVALID_ARG (unknown kv_dtype), those of fd_plan / fd_plan_sms.
  */
 int fd_plan_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max_len,

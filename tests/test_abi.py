@@ -198,7 +198,13 @@ def test_e4m3_plan_matches_bf16_rule_with_half_the_bytes(name, lib):
     w = WORKLOADS[name]
     p8, p16 = _plan_kv(w), _plan(w)
     assert p8.kv_dtype == fd.FD_KV_E4M3 and p16.kv_dtype == fd.FD_KV_BF16
-    assert p8.group_bytes == 1024 and p8.path == fd.FD_PATH_TC
+    assert p8.group_bytes == (1024 if w.HS == 256 else 2048) and p8.path == fd.FD_PATH_TC
+    # consumer warps: 8 for the E4M3 head-dim-512 MQA tile only when the grid
+    # is one block per SM; bf16 head dims 256/512 (16-row tiles) use 8
+    blocks = w.B * w.NKV * p8.num_splits
+    if w.HS == 512 and w.G > 8:
+        assert p8.consumer_warps == (8 if blocks <= 152 else 4)
+    assert p16.consumer_warps == (8 if w.HS == 256 or (w.HS == 512 and w.G > 8) else 4)
     # the same SM fill; a split is bounded by the same ~2 MiB of K+V bytes,
     # which at 2 bytes per position pair is twice the positions
     chunk8 = -(-p8.max_band // p8.num_splits)
@@ -216,7 +222,12 @@ def test_e4m3_plan_rejects_the_simt_path_and_unknown_types(lib):
         fd.fd_plan_override(p, 0, fd.FD_PATH_SIMT)
     assert e.value.status == fd.FD_ERR_INVALID_ARG
     fd.fd_plan_override(p, 9, fd.FD_PATH_TC)  # split count and clusters still move
-    assert p.num_splits == 9 and p.group_bytes == 1024
+    assert p.num_splits == 9 and p.group_bytes == 1024 and p.consumer_warps == 8
+    # the E4M3 MQA tile follows the grid: one block per SM -> 8 warps, more -> 4
+    m = _plan_kv(WORKLOADS["gemma_global_mqa_32k"])
+    assert m.num_splits * m.B * m.NKV <= 152 and m.consumer_warps == 8
+    fd.fd_plan_override(m, 2 * m.num_splits)
+    assert m.consumer_warps == 4
     pp = fd.fd_plan_t()
     assert lib.fd_plan_sms_kv(1, 16, 8, 256, 64, 0, 0, 152, 2, 8, 2, ctypes.byref(pp)) == fd.FD_ERR_INVALID_ARG
     assert lib.fd_plan_kv(1, 16, 8, 256, 64, 0, 0, 0, 7, ctypes.byref(pp)) == fd.FD_ERR_INVALID_ARG

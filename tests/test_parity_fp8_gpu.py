@@ -129,3 +129,18 @@ def test_fp8_full_size_workload_sampled_rows(name):
     del q, k8, v8
     torch.cuda.empty_cache()
     check(res, oracle_ref_fp8(w, qh, kh, vh, ksh, vsh, lens, rows=rows), rows=rows, what=name)
+
+
+def test_fp8_mqa_tile_both_warp_counts():
+    """The head-dim-512, 16-row E4M3 tile comes with eight consumer warps (grid
+    of at most one block per SM) and with four (more blocks): both match the
+    oracle."""
+    w = W("fp8_mqa_warps", 2, 16, 1, 512, 3000, 0, lens=(2999, 1234), seed=46)
+    q, k8, v8, ks, vs, lens = make_inputs_fp8(w)
+    ref = oracle_ref_fp8(w, q, k8, v8, ks, vs, lens)
+    seen = set()
+    for s in (8, 76, 100, 150):
+        res = run_fp8(w, q, k8, v8, ks, vs, lens, splits=s)
+        seen.add(res["plan"].consumer_warps)
+        check(res, ref, what=f"S={s} warps={res['plan'].consumer_warps}")
+    assert seen == {4, 8}
