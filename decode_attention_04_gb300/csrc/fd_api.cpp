@@ -139,7 +139,6 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   if (max_len > 0 && max_len < max_band) max_band = max_len;
   if (max_band < 1) max_band = 1;
 
-  const int granule = fd::plan_granule(path, HS);
   const long long units = static_cast<long long>(B > 0 ? B : 1) * NKV;
   // With large query groups a partial (G x HS floats) is costly next to a
   // split's K/V bytes, so fill each SM once rather than with every resident
@@ -148,6 +147,11 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   const long long slots = static_cast<long long>(num_sms) * (G >= 8 ? 1 : ctas_per_sm);
   long long s_fill = (slots + units - 1) / units;
   if (s_fill < 1) s_fill = 1;
+  // Whole-tile splits where filling the GPU would cut the band into pieces of
+  // under two tiles; longer pieces keep single positions as the granule, so
+  // rounding never leaves SMs idle.
+  const int tile = fd::plan_granule(path, HS, kv_dtype == FD_KV_E4M3);
+  const int granule = (max_band + s_fill - 1) / s_fill < 2 * tile ? tile : 1;
   auto chunk_for = [&](long long S) {
     long long c = (max_band + S - 1) / S;
     c = (c + granule - 1) / granule * granule;
@@ -360,9 +364,9 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
   if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
     return FD_ERR_INVALID_ARG;
   fd_plan_t p = *plan;
-  if (path != FD_PATH_AUTO) {
+  if (path != FD_PATH_AUTO && path != p.path) {
     p.path = path;
-    p.granule = fd::plan_granule(path, p.HS);
+    p.granule = 1;  // a forced kernel family walks single-position chunks
   }
   if (!valid_kv(p.kv_dtype, p.path)) return FD_ERR_INVALID_ARG;  // E4M3 runs on the tensor-core path only
   if (num_splits > 0) p.num_splits = num_splits;

@@ -39,8 +39,8 @@ struct LaunchArgs {
 
 // Positions per pipeline tile of the tensor-core kernel for head size HS, and
 // the chunk granule the plan uses for it.
-int tc_tile_positions(int HS);
-int plan_granule(int path, int HS);
+int tc_tile_positions(int HS, bool kv8);
+int plan_granule(int path, int HS, bool kv8);
 
 // Resident CTAs per SM of the kernel a plan would launch (occupancy query).
 cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas);

@@ -1277,23 +1277,22 @@ struct OccFn {
 
 }  // namespace
 
-int tc_tile_positions(int HS) {
+int tc_tile_positions(int HS, bool kv8) {
   switch (HS) {
-    case 64: return Tc64x1::T;
-    case 128: return Tc128x1::T;
-    case 256: return Tc256x1::T;
-    case 512: return Tc512x1::T;
+    case 64: return kv8 ? Tc64x1f::T : Tc64x1::T;
+    case 128: return kv8 ? Tc128x1f::T : Tc128x1::T;
+    case 256: return kv8 ? Tc256x1f::T : Tc256x1::T;
+    case 512: return kv8 ? Tc512x1f::T : Tc512x1::T;
     default: return 16;
   }
 }
 
-// Chunks need no rounding: rows are copied one by one, so a split may start at
-// any position, and a partial last tile is masked.
-int plan_granule(int path, int HS) {
-  (void)path;
-  (void)HS;
-  return 1;
-}
+// The whole-tile chunk granule of a kernel family: on the tensor-core path a
+// block's time is its tiles' latency chain, so a split shorter than a tile
+// costs as much as a full one while adding a partial to merge (measured on
+// GB300: a 256-position band ran 23% faster as 4 one-tile splits than as 37
+// splits of 7 positions). The SIMT kernel walks single positions.
+int plan_granule(int path, int HS, bool kv8) { return path == FD_PATH_SIMT ? 1 : tc_tile_positions(HS, kv8); }
 
 cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas) {
   if (path == FD_PATH_SIMT) {

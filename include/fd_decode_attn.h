@@ -103,9 +103,14 @@ enum {
  * units U = B * NKV; enough splits that U * num_splits covers every CTA slot of
  * the GPU once; a split then never exceeds `max_chunk` positions (a bound that
  * keeps ragged batches balanced), rounding num_splits up to a whole number of
- * waves when that bound applies. On the device each sequence cuts its own band
- * into chunks of ceil(band_b / num_splits) positions, so a short sequence
- * uses fewer, not emptier, splits.
+ * waves when that bound applies. Where filling the GPU would cut the band
+ * into pieces under two tiles of the tensor-core kernel, chunks are whole
+ * tiles (`granule` = the tile's positions: a split shorter than a tile costs
+ * a full tile's latency and adds a partial), so a short band gets fewer
+ * splits; otherwise the granule is 1. On
+ * the device each sequence cuts its own band into chunks of
+ * ceil(band_b / num_splits) positions rounded up to the granule, so a short
+ * sequence uses fewer, not emptier, splits.
  *
  * With G >= 8 query rows per KV head a partial (G x HS floats) is costly
  * next to a split's K/V bytes, and the plan fills each SM once instead of
@@ -133,7 +138,7 @@ typedef struct {
   int num_splits;          /* S: grid splits per (sequence, KV head) */
   int path;                /* FD_PATH_SIMT or FD_PATH_TC */
   int cluster;             /* blocks per cluster along the splits; divides S; 1 = none */
-  int granule;             /* chunk rounding on the device, positions */
+  int granule;             /* chunk rounding on the device, positions: 1, or the tile for short bands */
   int max_band;            /* band bound the plan was sized for */
   int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
   int num_sms;             /* SM count the plan assumed */
