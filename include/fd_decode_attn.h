@@ -259,8 +259,8 @@ int fd_decode_attn_ex(const fd_plan_t* plan, void* workspace, size_t workspace_b
  * fd_decode_attn / fd_decode_attn_ex; k8 and v8 must be 16-byte aligned and
  * the scales 4-byte aligned. Arithmetic: every E4M3 value is an fp16 value,
  * so codes widen to fp16 exactly; q is scaled by a power of two per block
- * (exact) and rounded to fp16 (exact for bf16 inputs within 2^-37 of the
- * block's largest |q|); products accumulate in fp32; the softmax weights
+ * (exact) and rounded to fp16 (exact for bf16 inputs within a factor 2^30
+ * of the block's largest |q|); products accumulate in fp32; the softmax weights
  * enter the P.V product as fp16 (relative error at most 2^-11 per weight);
  * O is multiplied by the V scale once at the end. fd_decode_attn_fp8_ex needs
  * an FD_KV_E4M3 plan (fd_plan_kv) and the bf16 entry points an FD_KV_BF16
