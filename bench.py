@@ -158,7 +158,7 @@ class Step:
     """L layers of one geometry resident on the device; kv = "bf16" or "e4m3"
     (E4M3 codes with per-(sequence, KV head) scales: half the live bytes)."""
 
-    def __init__(self, w, layers, device, seed_base=0, kv="bf16"):
+    def __init__(self, w, layers, device, seed_base=0, kv="bf16", path=0):
         from decode_attention_04_gb300.inputs import draw_lens, make_inputs, make_inputs_fp8
 
         self.w = w
@@ -180,9 +180,19 @@ class Step:
         self.lens = self.lens_h.to(device)
         self.out = [torch.empty_like(x) for x in self.q]
         self.live = live_band_bytes(w, self.lens_h) // (2 if kv == "e4m3" else 1)
+        # a forced kernel family runs through the explicit-workspace call
+        self.path = path
+        self.forced = None
+        if path:
+            import decode_attention_04_gb300 as fd
+            self.forced = self.plan()
+            fd.fd_plan_override(self.forced, 0, path)
+            self.ws = torch.zeros(max(16, self.forced.workspace_bytes), dtype=torch.uint8, device=device)
 
     def plan(self):
         import decode_attention_04_gb300 as fd
+        if getattr(self, "forced", None) is not None:
+            return self.forced
         w = self.w
         kv = fd.FD_KV_E4M3 if self.kv == "e4m3" else fd.FD_KV_BF16
         return fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, kv_dtype=kv)
@@ -190,6 +200,18 @@ class Step:
     def run(self, stream=None):
         import decode_attention_04_gb300 as fd
         w = self.w
+        if self.forced is not None:
+            p = self.forced
+            for i in range(self.L):
+                if self.kv == "e4m3":
+                    fd.fd_decode_attn_fp8_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
+                                             self.ks[i], self.vs[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
+                                             w.capacity, w.window, w.scale, stream)
+                else:
+                    fd.fd_decode_attn_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
+                                         self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
+                                         w.scale, stream)
+            return
         if self.kv == "e4m3":
             for i in range(self.L):
                 fd.fd_decode_attn_fp8(self.q[i], self.k[i], self.v[i], self.ks[i], self.vs[i], self.out[i],
@@ -280,6 +302,36 @@ def cpu_baseline(w, step: Step, budget_s: float = 10.0):
                       f"FP64, {cores} threads, {t_used:.2f} s"}
 
 
+def time_single_calls(step: Step, n: int, stream):
+    """Plain launches (no graph) of layer 0, one at a time: CUDA events around
+    each call, a synchronize between calls. Returns the median in µs."""
+    one = Step.__new__(Step)
+    one.__dict__.update(step.__dict__)
+    one.L = 1
+    ts = []
+    with torch.cuda.stream(stream):
+        for i in range(n + 3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one.run(stream)
+            b.record(stream)
+            stream.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
+
+
+def time_l2_hot(step: Step, steps: int, stream):
+    """A graph of layer 0 alone, replayed back to back: its K/V stay in L2 when
+    they fit (labelled L2-hot; not the metric). Returns µs per call."""
+    one = Step.__new__(Step)
+    one.__dict__.update(step.__dict__)
+    one.L = 1
+    ms, g = time_graph(one, steps, 3, stream)
+    del g
+    return statistics.median(ms) * 1e3
+
+
 def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
     from decode_attention_04_gb300.inputs import draw_lens
     lens = draw_lens(w)
@@ -292,10 +344,32 @@ def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
     gbs = st.live * L / (t * 1e-3) / 1e9
     res = {"us_per_layer": t * 1e3 / L, "us_per_layer_min": min(ms) * 1e3 / L, "live_GBps": gbs,
            "frac_of_peak": gbs / peak, "layers": L, "live_bytes_per_layer": st.live,
-           "num_splits": plan.num_splits, "desc": w.desc}
+           "num_splits": plan.num_splits, "desc": w.desc,
+           "us_single_call_plain_launch": time_single_calls(st, 20, stream),
+           "us_l2_hot_one_layer": time_l2_hot(st, steps, stream),
+           "l2_hot_fits": st.live <= L2_BYTES // 2}
     del st
     torch.cuda.empty_cache()
     return res
+
+
+def allocation_independence(steps, stream, device, caps=(4096, 32768, 131072)):
+    """Gemma global MQA at len 4096 with the cache allocated at several
+    capacities: the time must not grow with the allocation (the page's 537 MB
+    of whole-allocation reads was the bug this op fixes)."""
+    from dataclasses import replace
+    from decode_attention_04_gb300.inputs import WORKLOADS
+    base = WORKLOADS["gemma_global_mqa_4k"]
+    out = {}
+    for cap in caps:
+        w = replace(base, name=f"mqa_len4096_cap{cap}", capacity=cap)
+        L = 32  # 32 x 8.4 MB live > 2 x L2
+        st = Step(w, L, device)
+        ms, g = time_graph(st, steps, 3, stream)
+        out[str(cap)] = {"us_per_layer": statistics.median(ms) * 1e3 / L, "num_splits": st.plan().num_splits}
+        del st, g
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -311,6 +385,8 @@ def main():
                     help="profiling mode: N plain fd_decode_attn calls on one layer of --workload, then exit")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
                     help="cache type of --profile-calls (the timed step and its line are bf16)")
+    ap.add_argument("--path", type=int, default=0,
+                    help="kernel family of --profile-calls (0 = the plan's, 1 SIMT, 2 mma tiles, 3 tcgen05)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -323,7 +399,7 @@ def main():
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
     if args.profile_calls:
-        return profile_calls(w, args.profile_calls, args.kv)
+        return profile_calls(w, args.profile_calls, args.kv, args.path)
 
     import decode_attention_04_gb300 as fd
     from decode_attention_04_gb300 import build as libbuild
@@ -377,7 +453,7 @@ def main():
     live = step.live
     del graph
     clocks = clk.summary()
-    geoms = geoms8 = None
+    geoms = geoms8 = alloc = None
     if not args.no_geometries:
         del step
         torch.cuda.empty_cache()
@@ -386,6 +462,7 @@ def main():
             geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak)
         for name, gw in WORKLOADS.items():
             geoms8[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak, kv="e4m3")
+        alloc = allocation_independence(max(10, min(args.steps, 30)), stream, device)
 
     traffic = None
     tf = ROOT / "profiles" / "traffic.txt"
@@ -436,7 +513,8 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "geometries": geoms,
-        "geometries_e4m3": geoms8 if not args.no_geometries else None,
+        "geometries_e4m3": geoms8,
+        "allocation_independence": alloc,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -445,12 +523,12 @@ def main():
     return 0
 
 
-def profile_calls(w, n, kv="bf16"):
+def profile_calls(w, n, kv="bf16", path=0):
     """N plain calls on one layer (for ncu launch lists and captures)."""
     from decode_attention_04_gb300 import build as libbuild
     libbuild.build()
     device = torch.device("cuda", 0)
-    st = Step(w, 1, device, kv=kv)
+    st = Step(w, 1, device, kv=kv, path=path)
     for _ in range(n):
         st.run()
     torch.cuda.synchronize()

@@ -32,6 +32,7 @@ FD_DEVERR_WAIT_TIMEOUT = 1 << 2
 FD_PATH_AUTO = 0
 FD_PATH_SIMT = 1
 FD_PATH_TC = 2
+FD_PATH_UMMA = 3
 
 FD_KV_BF16 = 0
 FD_KV_E4M3 = 1

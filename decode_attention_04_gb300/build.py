@@ -22,7 +22,7 @@ BUILD_DIR = PKG / "_build"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", str(INCLUDE), "-I", str(CSRC)] + ARCH
-SOURCES = ["fd_kernels.cu", "fd_api.cpp", "fd_noalloc.cu"]
+SOURCES = ["fd_kernels.cu", "fd_umma.cu", "fd_api.cpp", "fd_noalloc.cu"]
 
 
 def nvcc() -> str:
@@ -36,7 +36,7 @@ def _stale() -> bool:
     if not LIB.exists():
         return True
     t = LIB.stat().st_mtime
-    deps = [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(INCLUDE.glob("*.h")) + [Path(__file__)]
+    deps = [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(CSRC.glob("*.cuh")) + list(INCLUDE.glob("*.h")) + [Path(__file__)]
     return any(d.stat().st_mtime > t for d in deps)
 
 

@@ -80,6 +80,7 @@ int fused_rule(const fd_plan_t& p) {
 int group_rule(const fd_plan_t& p) {
   const long long G = p.NH / p.NKV;
   const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
+  if (p.path == FD_PATH_UMMA) return 16384;  // one TMA box: 128 positions x 64 dims
   if (p.kv_dtype == FD_KV_E4M3) return p.HS == 256 ? 1024 : 2048;
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
 }
@@ -92,6 +93,7 @@ bool warps_choice_open(const fd_plan_t& p) {
 }
 
 int warps_rule(const fd_plan_t& p) {
+  if (p.path == FD_PATH_UMMA) return 4;  // softmax warps; one more issues the MMAs
   if (p.path != FD_PATH_TC) return 0;
   const bool two = p.NH / p.NKV > 8;
   if (p.kv_dtype == FD_KV_E4M3) {
@@ -114,6 +116,11 @@ void finish_plan(fd_plan_t* p, int fused = -1) {
 
 bool valid_kv(int kv_dtype, int path) {
   return kv_dtype == FD_KV_BF16 || (kv_dtype == FD_KV_E4M3 && path == FD_PATH_TC);
+}
+
+bool valid_path(const fd_plan_t& p) {
+  if (p.path == FD_PATH_TC || p.path == FD_PATH_SIMT) return true;
+  return p.path == FD_PATH_UMMA && p.kv_dtype == FD_KV_BF16 && fd::umma_shape_ok(p.HS, p.NH / p.NKV, p.window);
 }
 
 bool valid_cluster(int cluster, int num_splits, int HS, int path) {
@@ -360,7 +367,8 @@ int fd_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_le
 
 int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int fused) {
   if (!plan || num_splits < 0 || cluster < 0 || num_splits > 65535 * 64) return FD_ERR_INVALID_ARG;
-  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_TC) return FD_ERR_INVALID_ARG;
+  if (path != FD_PATH_AUTO && path != FD_PATH_SIMT && path != FD_PATH_TC && path != FD_PATH_UMMA)
+    return FD_ERR_INVALID_ARG;
   if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
     return FD_ERR_INVALID_ARG;
   fd_plan_t p = *plan;
@@ -368,7 +376,7 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
     p.path = path;
     p.granule = 1;  // a forced kernel family walks single-position chunks
   }
-  if (!valid_kv(p.kv_dtype, p.path)) return FD_ERR_INVALID_ARG;  // E4M3 runs on the tensor-core path only
+  if (!valid_kv(p.kv_dtype, p.path) || !valid_path(p)) return FD_ERR_INVALID_ARG;
   if (num_splits > 0) p.num_splits = num_splits;
   if (cluster > 0) p.cluster = cluster;
   if (p.path == FD_PATH_SIMT && cluster == 0) p.cluster = 1;  // the SIMT path has no clusters
@@ -394,14 +402,14 @@ int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int 
   if (plan->B != B || plan->NH != NH || plan->NKV != NKV || plan->HS != HS || plan->capacity != capacity ||
       plan->window != window || plan->kv_dtype != kv_dtype)
     return FD_ERR_INVALID_ARG;
-  if (plan->num_splits < 1 || (plan->path != FD_PATH_TC && plan->path != FD_PATH_SIMT) || plan->granule < 1 ||
-      !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
+  if (plan->num_splits < 1 || !valid_path(*plan) || plan->granule < 1 || !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
       (plan->fused && !fused_rule_allowed(*plan)))
     return FD_ERR_INVALID_ARG;
   if (plan->consumer_warps != warps_rule(*plan) &&
       !(warps_choice_open(*plan) && (plan->consumer_warps == 4 || plan->consumer_warps == 8)))
     return FD_ERR_INVALID_ARG;
-  if (kv_dtype == FD_KV_E4M3) return plan->group_bytes == group_rule(*plan) ? FD_OK : FD_ERR_INVALID_ARG;
+  if (kv_dtype == FD_KV_E4M3 || plan->path == FD_PATH_UMMA)
+    return plan->group_bytes == group_rule(*plan) ? FD_OK : FD_ERR_INVALID_ARG;
   if ((plan->group_bytes != 2048 && plan->group_bytes != 4096) ||
       (plan->group_bytes == 4096 && group_rule(*plan) != 4096 &&
        !(plan->HS == 512 && plan->NH / plan->NKV > 8 && plan->path == FD_PATH_TC)))

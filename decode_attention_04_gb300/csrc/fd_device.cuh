@@ -1,0 +1,182 @@
+// Device-side helpers shared by the split kernels (fd_kernels.cu, fd_umma.cu):
+// the band and chunk rules, bf16 bit conversions, mbarrier waits that give up
+// after about a second, bulk copies, programmatic dependent launch, cluster
+// and proxy fences. Included inside `namespace fd { namespace { ... } }`, so
+// every translation unit gets its own copy, including its own device error
+// word `g_device_error` (read back by that unit's host code).
+#pragma once
+
+__device__ unsigned int g_device_error;
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Live band of sequence b: positions [lo, lo + band). Reports repaired
+// lengths through the device error word when `report` is set.
+__device__ __forceinline__ int band_of(int len, int capacity, int window, bool report, int* lo) {
+  unsigned flags = 0;
+  if (len < 0) {
+    flags |= FD_DEVERR_LEN_NEGATIVE;
+    len = 0;
+  }
+  int keep = capacity;
+  if (window > 0) {
+    keep = min(window, capacity);
+  } else if (len > capacity) {
+    flags |= FD_DEVERR_LEN_CLAMPED;
+  }
+  const int l0 = max(0, len - keep);
+  if (report && flags) atomicOr(&g_device_error, flags);
+  *lo = l0;
+  return len - l0;
+}
+
+// Positions per split for a band: ceil(band / S) rounded up to the granule.
+__device__ __forceinline__ int chunk_of(int band, int num_splits, int granule) {
+  const long long c = (static_cast<long long>(band) + num_splits - 1) / num_splits;
+  const long long r = ((c + granule - 1) / granule) * granule;
+  return static_cast<int>(r < granule ? granule : r);
+}
+
+__device__ __forceinline__ int active_splits(int band, int chunk) {
+  return band <= 0 ? 0 : (band + chunk - 1) / chunk;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after about one second of wall time, raises
+// FD_DEVERR_WAIT_TIMEOUT and returns false. `failed` is sticky per thread, so
+// after one timeout every later wait of that thread returns at once and the
+// kernel runs to its end; no wait in this library can hang the GPU.
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& failed) {
+  if (failed) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+  }
+  failed = true;
+  atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);
+  return false;
+}
+
+// 1-D bulk async copy global -> this CTA's shared memory, completing bytes on
+// the mbarrier. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start while the
+// previous kernel on the stream is still running. It must wait for that
+// kernel (and its memory) before reading any input; it lets the next kernel
+// launch once every one of its own blocks has started. Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Thread-block clusters: rank of this block in its cluster, another block's
+// shared-memory address, loads through distributed shared memory, and a
+// barrier over every thread of the cluster (release/acquire, so shared-memory
+// writes before it are visible to the whole cluster after it).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+

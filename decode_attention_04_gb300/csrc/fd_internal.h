@@ -33,7 +33,7 @@ struct LaunchArgs {
   int num_splits;           // S
   int cluster;              // blocks per cluster along the splits (S % cluster == 0)
   int granule;              // chunk rounding, positions
-  int path;                 // FD_PATH_SIMT / FD_PATH_TC
+  int path;                 // FD_PATH_SIMT / FD_PATH_TC / FD_PATH_UMMA
   float scale_log2;         // scale * log2(e)
 };
 
@@ -48,6 +48,13 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas);
 // Largest cluster size (16, 8, ... 1) of the tensor-core split kernel that the
 // device can schedule (cluster occupancy query).
 cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster);
+
+// The tcgen05 / tensor-memory split kernel (fd_umma.cu): bf16, head dim 512,
+// 8 < G <= 16 query rows per KV head, no window.
+bool umma_shape_ok(int HS, int G, int window);
+int umma_tile_positions();
+cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream);
+cudaError_t read_and_clear_device_error_umma(unsigned int* err);
 
 // Launch the split kernel (and the merge kernel when S > 1) on `stream`.
 cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);

@@ -89,7 +89,9 @@ enum {
 enum {
   FD_PATH_AUTO = 0,   /* let the plan choose */
   FD_PATH_SIMT = 1,   /* plain per-position fp32 kernel; reference GPU path */
-  FD_PATH_TC = 2      /* bulk-copy pipelined, tensor-core (mma) tile kernel */
+  FD_PATH_TC = 2,     /* bulk-copy pipelined, tensor-core (mma) tile kernel */
+  FD_PATH_UMMA = 3    /* TMA + tcgen05 kernel, accumulators in tensor memory: bf16,
+                         HS 512, 8 < G <= 16, window <= 0 */
 };
 
 /*
