@@ -287,10 +287,34 @@ struct TcCfg {
   static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
 
+constexpr int kLptMaxB = 64;
+
+// The sequence that blocks with blockIdx.z == z work on: the z-th longest band
+// (ties by index) when 1 < B <= kLptMaxB, else z itself. Blocks start in
+// blockIdx order, so the longest splits start first and the last wave holds
+// the short ones (longest-processing-time-first order); every order gives the
+// same partials. Every thread of the block calls it (it synchronises).
+__device__ int lpt_sequence(const LaunchArgs& a, int z, int tid, int nthreads, int* s_seq) {
+  if (a.B <= 1 || a.B > kLptMaxB) return z;
+  int lo;
+  for (int t = tid; t < a.B; t += nthreads) {
+    const int bt = band_of(a.lens[t], a.capacity, a.window, false, &lo);
+    int rank = 0;
+    for (int u = 0; u < a.B; ++u) {
+      const int bu = band_of(a.lens[u], a.capacity, a.window, false, &lo);
+      rank += (bu > bt) || (bu == bt && u < t);
+    }
+    s_seq[rank] = t;
+  }
+  __syncthreads();
+  return s_seq[z];
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  __shared__ int s_seq[kLptMaxB];
+  const int s = blockIdx.x, kvh = blockIdx.y;
   const int G = a.NH / a.NKV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hbase = kvh * G;
@@ -321,6 +345,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   grid_dependency_wait();
   grid_launch_dependents();
+  const int b = lpt_sequence(a, blockIdx.z, tid, C::THREADS, s_seq);
 
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
