@@ -42,43 +42,59 @@ namespace {
 namespace um {
 constexpr int HS = 512;                 // head dim
 constexpr int NQ = 16;                  // query rows per MMA (N); G <= 16, zero rows above G
-constexpr int T = 128;                  // positions per tile (MMA M)
 constexpr int DC = 64;                  // head dims per chunk: one 128-byte swizzle row
 constexpr int NCH = HS / DC;            // chunks per tensor per tile
-constexpr int CHUNK_BYTES = T * DC * 2; // 16 KB
-constexpr int NRING = 10;               // even, so a V chunk pair never straddles the wrap
 constexpr int TAIL_ROWS = 8;            // box height for a tile's partial rows
 constexpr int NSOFT = 4;                // softmax warps: 2..5, one TMEM lane quarter each
 constexpr int THREADS = (2 + NSOFT) * 32;
 constexpr int ATOM_Q = NQ * 128;        // 16 rows x 128 B: one K-major swizzle column of Q or P
-// shared memory, from a 1024-byte aligned base
-constexpr int OFF_RING = 0;
-constexpr int OFF_Q = OFF_RING + NRING * CHUNK_BYTES;  // Q: NCH atoms of 16 rows x 64 dims
-constexpr int OFF_P = OFF_Q + NCH * ATOM_Q;            // P: [2 buffers][hi, lo][2 atoms]
-constexpr int P_HALF = 2 * ATOM_Q;                     // 128 positions of one half (hi or lo)
-constexpr int P_BUF = 2 * P_HALF;                      // hi + lo
-constexpr int OFF_RED = OFF_P + 2 * P_BUF;             // f32 [2][NQ][NSOFT] row maxima, row sums
-constexpr int OFF_BAR = OFF_RED + 2 * NQ * NSOFT * 4;
-// full[NRING], empty[NRING], q_ready, s_full[2], p_ready[2], pv_done
-constexpr int NBAR = 2 * NRING + 6;
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;           // u32: tensor memory base address
-constexpr int SMEM = OFF_TMEM + 16 + 1024;             // + slack to align the base
-constexpr uint32_t TMEM_COLS = 128;                    // S[2] at columns 0, 16; O block mb at 32 + 16 mb
+constexpr int RING_BYTES = 160 * 1024;  // the K/V chunk ring
+constexpr uint32_t TMEM_COLS = 128;     // S[2] at columns 0, 16; O block mb at 32 + 16 mb
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5 = 1), A and
 // B bf16 (bits 7-9, 10-12 = 1), A MN-major when bit 15 is set, N / 8 at bits
 // 17-22, M / 16 at bits 24-28.
-constexpr uint32_t idesc_bf16(bool a_mn_major) {
+constexpr uint32_t idesc_bf16(bool a_mn_major, int M) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         (static_cast<uint32_t>(NQ >> 3) << 17) | (static_cast<uint32_t>(T >> 4) << 24);
+         (static_cast<uint32_t>(NQ >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc_bf16(false);  // A = K tile, K-major (dims contiguous)
-constexpr uint32_t kIdescPV = idesc_bf16(true);   // A = V^T, MN-major (dims contiguous)
-
-static_assert(SMEM <= 227 * 1024, "shared memory");
-static_assert(NRING % 2 == 0 && NRING >= NCH, "ring");
-static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+constexpr uint32_t kIdescPV = idesc_bf16(true, 128);  // A = V^T, MN-major (dims contiguous), M = 128 dims
 }  // namespace um
+
+// Tile-dependent layout: T positions per tile (the score MMA's M, 64 or 128).
+// An M = 128 accumulator keeps row r in tensor-memory lane r; an M = 64 one
+// keeps row r in lane 32 (r / 16) + r % 16 (the first 16 lanes of each
+// warp's quarter). P.V always runs with M = 128 head dims.
+template <int T_>
+struct UmmaTile {
+  static constexpr int T = T_;
+  static constexpr int CHUNK_BYTES = T * um::DC * 2;             // one TMA box: T positions x 64 dims
+  static constexpr int NRING = um::RING_BYTES / CHUNK_BYTES;     // even: a V chunk pair never straddles the wrap
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_Q = OFF_RING + NRING * CHUNK_BYTES;   // Q: NCH atoms of 16 rows x 64 dims
+  static constexpr int OFF_P = OFF_Q + um::NCH * um::ATOM_Q;     // P: [2 buffers][hi, lo][T / 64 atoms]
+  static constexpr int P_HALF = (T / 64) * um::ATOM_Q;          // T positions of one half (hi or lo)
+  static constexpr int P_BUF = 2 * P_HALF;                       // hi + lo
+  static constexpr int OFF_RED = OFF_P + 2 * P_BUF;              // f32 [2][NQ][NSOFT] row maxima, row sums
+  static constexpr int OFF_BAR = OFF_RED + 2 * um::NQ * um::NSOFT * 4;
+  // full[NRING], empty[NRING], q_ready, s_full[2], p_ready[2], pv_done
+  static constexpr int NBAR = 2 * NRING + 6;
+  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;            // u32: tensor memory base address
+  static constexpr int SMEM = OFF_TMEM + 16 + 1024;              // + slack to align the base
+  static constexpr int LPQ = T / 4;                              // S rows per warp lane quarter
+  static constexpr uint32_t kIdescQK = um::idesc_bf16(false, T); // A = K tile, K-major (dims contiguous)
+
+  static_assert(T == 64 || T == 128, "score MMA M");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static_assert(NRING % 2 == 0 && NRING >= um::NCH, "ring");
+  static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+};
+
+// Positions per tile of the kernel the library launches. Measured on GB300
+// (µs per layer, MQA 32k / MQA long at 38 splits): T = 128 26.6 / 189,
+// T = 64 35.2 / 321. A tile's time is mostly its fixed chain (softmax, MMA
+// commits, P.V before the next scores), so halving the tile doubles it.
+constexpr int kUmmaTile = 128;
 
 // Shared-memory matrix descriptor (tcgen05): start address / 16 in bits
 // 0-13, leading-dimension byte offset / 16 in 16-29, stride-dimension byte
@@ -215,9 +231,15 @@ struct UmmaMaps {
   CUtensorMap k_tail, v_tail;  // boxes of 64 dims x 8 rows
 };
 
+template <int T_>
 __global__ void __launch_bounds__(um::THREADS, 1)
     split_umma_kernel(const __grid_constant__ UmmaMaps maps, const LaunchArgs a) {
   using namespace um;
+  using U = UmmaTile<T_>;
+  constexpr int T = U::T, CHUNK_BYTES = U::CHUNK_BYTES, NRING = U::NRING, OFF_RING = U::OFF_RING;
+  constexpr int OFF_Q = U::OFF_Q, OFF_P = U::OFF_P, P_HALF = U::P_HALF, P_BUF = U::P_BUF, OFF_RED = U::OFF_RED;
+  constexpr int OFF_BAR = U::OFF_BAR, OFF_TMEM = U::OFF_TMEM, LPQ = U::LPQ;
+  constexpr uint32_t kIdescQK = U::kIdescQK;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -397,7 +419,10 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     const int sw = warp - 2;             // 0..3
     const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
     const int tq = tid - 64;             // 0..127
-    const int pl = quarter * 32 + lane;  // tile position (TMEM lane) this thread owns
+    // tile position whose S row this thread's TMEM lane holds (lanes >= LPQ of
+    // a quarter hold none when T = 64)
+    const bool lane_ok = lane < LPQ;
+    const int pl = quarter * LPQ + (lane & (LPQ - 1));
     const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
 
     // Q -> shared memory as the K-major, 128-byte-swizzled B operand: atom c
@@ -433,7 +458,7 @@ __global__ void __launch_bounds__(um::THREADS, 1)
       tc_fence_after();
       float sc[NQ];
       tmem_ld16(tmem + tlane + 16 * (i & 1), sc);
-      const bool valid = pl < nv;
+      const bool valid = lane_ok && pl < nv;
 #pragma unroll
       for (int r = 0; r < NQ; ++r) sc[r] = valid ? sc[r] * a.scale_log2 : kNegInf;
 
@@ -455,13 +480,15 @@ __global__ void __launch_bounds__(um::THREADS, 1)
       {
         unsigned char* pbuf = smem + OFF_P + (i & 1) * P_BUF + (pl >> 6) * ATOM_Q;
         const int pc = (pl & 63) >> 3, pw = (pl & 7) * 2;
+        if (lane_ok) {
 #pragma unroll
-        for (int r = 0; r < NQ; ++r) {
-          const uint16_t hi = f32_to_bf16_bits(p[r]);
-          const uint16_t lo = f32_to_bf16_bits(p[r] - bf16_bits_to_f32(hi));
-          unsigned char* at = pbuf + (r >> 3) * 1024 + (r & 7) * 128 + ((pc ^ (r & 7)) << 4) + pw;
-          *reinterpret_cast<uint16_t*>(at) = hi;
-          *reinterpret_cast<uint16_t*>(at + P_HALF) = lo;
+          for (int r = 0; r < NQ; ++r) {
+            const uint16_t hi = f32_to_bf16_bits(p[r]);
+            const uint16_t lo = f32_to_bf16_bits(p[r] - bf16_bits_to_f32(hi));
+            unsigned char* at = pbuf + (r >> 3) * 1024 + (r & 7) * 128 + ((pc ^ (r & 7)) << 4) + pw;
+            *reinterpret_cast<uint16_t*>(at) = hi;
+            *reinterpret_cast<uint16_t*>(at + P_HALF) = lo;
+          }
         }
       }
 
@@ -508,7 +535,7 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     for (int mb = 0; mb < NCH / 2; ++mb) {
       float o[NQ];
       tmem_ld16(tmem + tlane + 32 + 16 * mb, o);
-      const int d = mb * 128 + pl;
+      const int d = mb * 128 + quarter * 32 + lane;  // O^T lanes are head dims
 #pragma unroll
       for (int r = 0; r < NQ; ++r) {
         if (r >= G) break;
@@ -578,29 +605,31 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const LaunchArgs& a, uin
 
 bool umma_shape_ok(int HS, int G, int window) { return HS == um::HS && G > 8 && G <= um::NQ && window <= 0; }
 
-int umma_tile_positions() { return um::T; }
+int umma_tile_positions() { return kUmmaTile; }
 
 cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream) {
   if (!umma_shape_ok(a.HS, a.NH / a.NKV, a.window) || a.cluster != 1 || a.fused || a.kv8 ||
       static_cast<long long>(a.B) * a.NKV * a.capacity >= (1ll << 31))
     return cudaErrorInvalidValue;
   UmmaMaps maps;
-  if (!encode_cache_map(&maps.k, a.k, a, um::T) || !encode_cache_map(&maps.v, a.v, a, um::T) ||
+  if (!encode_cache_map(&maps.k, a.k, a, kUmmaTile) || !encode_cache_map(&maps.v, a.v, a, kUmmaTile) ||
       !encode_cache_map(&maps.k_tail, a.k, a, um::TAIL_ROWS) || !encode_cache_map(&maps.v_tail, a.v, a, um::TAIL_ROWS))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(split_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, um::SMEM);
+  constexpr int kSmem = UmmaTile<kUmmaTile>::SMEM;
+  cudaError_t e =
+      cudaFuncSetAttribute(split_umma_kernel<kUmmaTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.num_splits, a.NKV, a.B);
   cfg.blockDim = dim3(um::THREADS);
-  cfg.dynamicSmemBytes = um::SMEM;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_umma_kernel, maps, a);
+  return cudaLaunchKernelEx(&cfg, split_umma_kernel<kUmmaTile>, maps, a);
 }
 
 cudaError_t read_and_clear_device_error_umma(unsigned int* err) {
