@@ -254,3 +254,45 @@ def test_e4m3_argument_errors_before_any_cuda_call(lib):
     bad = (1, 16, 8, 96, 64, 0, 0.0, None)
     assert lib.fd_decode_attn_fp8(A, A, A, A, A, A, A, *bad) == fd.FD_ERR_UNSUPPORTED
     assert lib.fd_decode_attn_fp8(A, A, A, None, A, A, A, *args) == fd.FD_ERR_INVALID_ARG
+
+
+def test_short_bands_split_into_whole_tiles(lib):
+    """Where filling the GPU would cut the band into pieces under two tiles,
+    the chunk granule is the tile (64 positions at d128, 32 at d256), so a
+    split is never a sliver of a tile; long bands keep granule 1."""
+    tiny, ring = _plan(WORKLOADS["llama_tiny"]), _plan(WORKLOADS["gemma_local_ring"])
+    assert tiny.granule == 64 and ring.granule == 32
+    for p in (tiny, ring):
+        chunk = -(-p.max_band // p.num_splits)
+        chunk = -(-chunk // p.granule) * p.granule
+        assert chunk % p.granule == 0 and chunk >= p.granule
+    assert ring.num_splits == 32  # 1024 / 32: one tile per split
+    for name in ("gemma_global_mqa_32k", "llama_ragged", "gemma_mqa_long"):
+        assert _plan(WORKLOADS[name]).granule == 1
+    # a forced split count keeps the plan's granule; a forced family resets it
+    p = _plan(WORKLOADS["llama_tiny"])
+    fd.fd_plan_override(p, 3)
+    assert p.granule == 64
+    fd.fd_plan_override(p, 0, fd.FD_PATH_SIMT)
+    assert p.granule == 1
+
+
+def test_tcgen05_family_is_opt_in_and_shape_bound(lib):
+    """Plans never pick FD_PATH_UMMA; it is accepted for bf16, head dim 512,
+    8 < G <= 16 and no window, with its own copy-group and warp fields."""
+    for name in WORKLOADS:
+        assert _plan(WORKLOADS[name]).path == fd.FD_PATH_TC
+    p = _plan(WORKLOADS["gemma_global_mqa_32k"])
+    fd.fd_plan_override(p, 0, fd.FD_PATH_UMMA)
+    assert p.path == fd.FD_PATH_UMMA and p.group_bytes == 16384 and p.consumer_warps == 4
+    for w in (WORKLOADS["gemma_local_ring"], WORKLOADS["llama_tiny"]):
+        q = _plan(w)
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_override(q, 0, fd.FD_PATH_UMMA)
+    e = _plan_kv(WORKLOADS["gemma_global_mqa_32k"])
+    with pytest.raises(fd.FdError):
+        fd.fd_plan_override(e, 0, fd.FD_PATH_UMMA)  # bf16 only
+    for bad in [(0, fd.FD_PATH_UMMA, 2), (0, fd.FD_PATH_UMMA, 0, 1)]:
+        q = fd.fd_plan_t.from_buffer_copy(p)
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_override(q, *bad)
