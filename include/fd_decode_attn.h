@@ -129,6 +129,16 @@ enum {
  * 4 KB groups (a tile that needs the whole SM's shared memory): fewer copies
  * per block, and a block's copy rate is set by its copy count.
  *
+ * Tensor-memory kernel (opt-in through fd_plan_override(..., FD_PATH_UMMA, ...);
+ * plans never choose it): for the MQA geometry of "One KV head breaks the
+ * textbook" (bf16, HS 512, 8 < G <= 16, window <= 0) the split blocks stream
+ * K and V as 128-position TMA tiles and run S^T = K Q^T and O^T += V^T P^T as
+ * tcgen05 MMAs with the accumulators in tensor memory; with no window the
+ * band's slots are [0, min(len, capacity)), walked in slot order. Such a plan
+ * has group_bytes = 16384 (one TMA box), consumer_warps = 4, cluster = 1 and
+ * no fused merge; the merge kernel is the same. Measured slower than
+ * FD_PATH_TC on GB300 (the 256 KB tile outgrows the shared-memory ring).
+ *
  * Clusters (opt-in through fd_plan_override; plans use cluster = 1): the
  * blocks of `cluster` consecutive splits form a thread-block cluster and
  * combine their partials through distributed shared memory, so only
@@ -191,7 +201,8 @@ int fd_plan_sms_kv(int B, int NH, int NKV, int HS, int capacity, int window, int
 
 /*
  * fd_plan_override: force the split count (num_splits >= 1; 0 keeps the
- * plan's), the kernel family (path != FD_PATH_AUTO), the cluster size
+ * plan's), the kernel family (path != FD_PATH_AUTO; FD_PATH_UMMA only for the
+ * shapes above), the cluster size
  * (cluster >= 1, a power of two <= 16 that divides num_splits and HS / 4;
  * 0 keeps the plan's; the SIMT path takes cluster 1 only) and/or the fused
  * merge (fused = 0 off, 1 on where allowed, -1 the plan's rule), then
