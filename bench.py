@@ -85,7 +85,9 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi every 200 ms while the timed region runs."""
+    """Samples nvidia-smi every 20 ms while the timed regions run; entering
+    waits (up to 5 s) for the first sample so the sampler is live before the
+    timed region starts."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -95,14 +97,19 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.skip = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.skip = len(self.lines)  # samples taken before the timed region are not counted
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
@@ -125,7 +132,7 @@ class ClockSampler:
             return None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.skip:]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -433,7 +440,9 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ms, graph = time_graph(step, args.steps, args.warmup, stream)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        # ---- end to end through the public call, host buffers (sampled too)
+        e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
     tot_ms = max_over_ranks(sum(ms), device)
     if world > 1:
         import torch.distributed as dist
@@ -442,9 +451,6 @@ def main():
     value = job_gbps(step.live * L, world, ms_per_step)
     per_layer_us = ms_per_step * 1e3 / L
     achieved = step.live / (per_layer_us * 1e-6) / 1e9
-
-    # ---- end to end through the public call, host buffers
-    e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
     e2e_ms_per_step = max_over_ranks(statistics.mean(e2e_ms), device)
     e2e_value = job_gbps(step.live * L, world, e2e_ms_per_step)
 
