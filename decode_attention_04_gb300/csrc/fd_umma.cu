@@ -605,8 +605,6 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const LaunchArgs& a, uin
 
 bool umma_shape_ok(int HS, int G, int window) { return HS == um::HS && G > 8 && G <= um::NQ && window <= 0; }
 
-int umma_tile_positions() { return kUmmaTile; }
-
 cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream) {
   if (!umma_shape_ok(a.HS, a.NH / a.NKV, a.window) || a.cluster != 1 || a.fused || a.kv8 ||
       static_cast<long long>(a.B) * a.NKV * a.capacity >= (1ll << 31))
