@@ -438,15 +438,19 @@ def main():
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    def bracket():  # a barrier and a device synchronize on each side of a timed region
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
     with ClockSampler(local) as clk:
         ms, graph = time_graph(step, args.steps, args.warmup, stream)
-        torch.cuda.synchronize()
+        bracket()
         # ---- end to end through the public call, host buffers (sampled too)
         e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
+        bracket()
     tot_ms = max_over_ranks(sum(ms), device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
     ms_per_step = tot_ms / args.steps
     value = job_gbps(step.live * L, world, ms_per_step)
     per_layer_us = ms_per_step * 1e3 / L
