@@ -229,7 +229,7 @@ class Step:
                               w.capacity, w.window, w.scale, stream)
 
 
-def time_graph(step: Step, steps: int, warmup: int, stream):
+def time_graph(step: Step, steps: int, warmup: int, stream, bracket=None):
     """Capture the L-layer step in a CUDA graph; time `steps` replays with CUDA
     events on the capture stream. Returns per-step milliseconds (list)."""
     with torch.cuda.stream(stream):
@@ -243,6 +243,8 @@ def time_graph(step: Step, steps: int, warmup: int, stream):
         for _ in range(max(3, warmup)):
             g.replay()
     stream.synchronize()
+    if bracket:
+        bracket()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
@@ -253,7 +255,7 @@ def time_graph(step: Step, steps: int, warmup: int, stream):
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)], g
 
 
-def time_e2e(step: Step, steps: int, warmup: int, stream):
+def time_e2e(step: Step, steps: int, warmup: int, stream, bracket=None):
     """Each step: pinned host Q (all layers) and lens -> device, the L public
     calls, outputs -> pinned host; CUDA events around the whole step."""
     w = step.w
@@ -277,6 +279,8 @@ def time_e2e(step: Step, steps: int, warmup: int, stream):
         for _ in range(max(3, warmup)):
             one()
         stream.synchronize()
+        if bracket:
+            bracket()
         ev[0].record(stream)
         for i in range(steps):
             one()
@@ -445,10 +449,10 @@ def main():
             dist.barrier()
 
     with ClockSampler(local) as clk:
-        ms, graph = time_graph(step, args.steps, args.warmup, stream)
+        ms, graph = time_graph(step, args.steps, args.warmup, stream, bracket)
         bracket()
         # ---- end to end through the public call, host buffers (sampled too)
-        e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream)
+        e2e_ms, h2d, d2h = time_e2e(step, args.steps, args.warmup, stream, bracket)
         bracket()
     tot_ms = max_over_ranks(sum(ms), device)
     ms_per_step = tot_ms / args.steps
