@@ -144,3 +144,22 @@ def test_fp8_mqa_tile_both_warp_counts():
         seen.add(res["plan"].consumer_warps)
         check(res, ref, what=f"S={s} warps={res['plan'].consumer_warps}")
     assert seen == {4, 8}
+
+
+@pytest.mark.parametrize("q_mul,k_mul,v_mul", [(1e4, 1.0, 1.0), (1e-3, 1.0, 1.0), (1.0, 1e-3, 1e3), (30.0, 8.0, 1e-2)],
+                         ids=["q_large", "q_tiny", "k_small_v_large", "peaked"])
+def test_fp8_extreme_magnitudes(q_mul, k_mul, v_mul):
+    """The per-block power-of-two Q scale and the folded K scale keep scores
+    exact in fp32 and finite for very large / small inputs; the V scale
+    multiplies O once. Checked against the oracle on the same codes and
+    scales (the fp32 tolerance is relative to the output's scale here)."""
+    w = W("fp8_extreme", 2, 16, 2, 256, 300, 0, lens=(300, 77), seed=47)
+    q, k8, v8, ks, vs, lens = make_inputs_fp8(w)
+    q = (q.float() * q_mul).to(torch.bfloat16)
+    ks, vs = ks * k_mul, vs * v_mul
+    res = run_fp8(w, q, k8, v8, ks, vs, lens)
+    ref = oracle_ref_fp8(w, q, k8, v8, ks, vs, lens)
+    got = res["out32"].double().numpy()
+    assert np.isfinite(got).all()
+    tol = 2e-3 * max(1.0, v_mul)
+    assert np.abs(got - ref).max() <= tol, np.abs(got - ref).max()

@@ -280,3 +280,15 @@ def test_full_size_workload_sampled_rows(name):
     torch.cuda.empty_cache()
     ref = oracle_ref(w, qh, kh, vh, lens, rows=rows)
     check(res, ref, rows=rows, what=name)
+
+
+@pytest.mark.parametrize("q_mul", [64.0, 1e-4], ids=["peaked", "flat"])
+def test_extreme_score_scales_match_oracle(q_mul):
+    """Very peaked (scores in the hundreds) and nearly flat softmaxes, on both
+    kernel families: the max shift and the hi/lo P split keep the tolerance."""
+    w = W("extreme", 2, 16, 8, 128, 400, 0, lens=(400, 133), seed=48)
+    q, k, v, lens = make_inputs(w)
+    q = (q.float() * q_mul).to(torch.bfloat16)
+    ref = oracle_ref(w, q, k, v, lens)
+    for path in (fd.FD_PATH_TC, fd.FD_PATH_SIMT):
+        check(run(w, q, k, v, lens, path=path), ref, what=f"q x {q_mul} path {path}")
