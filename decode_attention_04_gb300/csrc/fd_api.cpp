@@ -65,9 +65,10 @@ bool fused_rule_allowed(const fd_plan_t& p) {
 }
 
 // Off by default: measured on GB300, the separate merge kernel (already
-// resident through programmatic dependent launch, 128+ blocks pulling the
-// partials in parallel) beat the last block merging alone on every workload
-// here. Kept as an option (fd_plan_override) and tested both ways.
+// resident through programmatic dependent launch) beat the last block's fence,
+// counter and merge on the small bands (ring 7.32 vs 8.95 us per layer, llama
+// tiny 5.89 vs 6.88) and tied on the ragged batch. Kept as an option
+// (fd_plan_override) and tested both ways.
 int fused_rule(const fd_plan_t& p) {
   (void)p;
   return 0;

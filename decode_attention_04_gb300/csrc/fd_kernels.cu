@@ -782,34 +782,74 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       if (lane == 0) sLt[g] = L;
     }
     named_bar_sync(1, C::CTHREADS);
+    // O = sum_j w_j O_j / L per (row, 4 dims). When there are fewer such items
+    // than threads, each item's splits are divided among JG threads, so every
+    // thread has all its loads in flight at once; their sums meet in shared
+    // memory behind the weights.
     constexpr int D4 = C::HS / 4;
-    for (int it = tid; it < G * D4; it += C::CTHREADS) {
-      const int g = it / D4, d = (it % D4) * 4;
+    constexpr int kFusedBatch = 16;
+    const int items = G * D4;
+    int JG = C::CTHREADS / items;
+    if (JG < 1 || 512 + 4 * C::CTHREADS > C::NWC * C::NP * C::SP) JG = 1;
+    float4* sAcc = reinterpret_cast<float4*>(sS + 512);  // [JG][items], after sW (G * nsplit <= 480)
+    for (int t = tid; t < items * JG; t += C::CTHREADS) {
+      const int item = t % items, jg = t / items;
+      const int g = item / D4, d = (item % D4) * 4;
       const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
       const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * S * C::HS + d);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j0 = 0; j0 < nsplit; j0 += 8) {  // 8 loads in flight per thread
-        float4 v[8];
+      for (int j0 = jg; j0 < nsplit; j0 += kFusedBatch * JG) {
+        float4 v[kFusedBatch];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = j0 + u < nsplit ? __ldcg(src + static_cast<size_t>(j0 + u) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kFusedBatch; ++u) {
+          const int j = j0 + u * JG;
+          v[u] = j < nsplit ? __ldcg(src + static_cast<size_t>(j) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float w = j0 + u < nsplit ? sW[g * nsplit + j0 + u] : 0.f;
+        for (int u = 0; u < kFusedBatch; ++u) {
+          const int j = j0 + u * JG;
+          const float w = j < nsplit ? sW[g * nsplit + j] : 0.f;
           acc.x += w * v[u].x;
           acc.y += w * v[u].y;
           acc.z += w * v[u].z;
           acc.w += w * v[u].w;
         }
       }
-      const float L = sLt[g];
-      const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
-      const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
-                           (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
-      const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
-                           (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
-      *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
-      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+      if (JG > 1) {
+        sAcc[jg * items + item] = acc;
+      } else {
+        const float L = sLt[g];
+        const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+        const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                             (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+        const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                             (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+        *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+      }
+    }
+    if (JG > 1) {
+      named_bar_sync(1, C::CTHREADS);
+      for (int item = tid; item < items; item += C::CTHREADS) {
+        const int g = item / D4, d = (item % D4) * 4;
+        const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
+        float4 acc = sAcc[item];
+        for (int jg = 1; jg < JG; ++jg) {  // fixed order: the result does not depend on timing
+          const float4 o2 = sAcc[jg * items + item];
+          acc.x += o2.x;
+          acc.y += o2.y;
+          acc.z += o2.z;
+          acc.w += o2.w;
+        }
+        const float L = sLt[g];
+        const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+        const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                             (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+        const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                             (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+        *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+      }
     }
     return;
   }
