@@ -348,6 +348,43 @@ def time_l2_hot(step: Step, steps: int, stream):
     return statistics.median(ms) * 1e3
 
 
+def cpu_oracle_sample(w, step: Step, budget_s: float = 1.5):
+    """The FP64 oracle on layer 0 of a geometry, on all host cores and on one
+    thread: the first k (sequence, head) rows, k sized from one timed row so
+    each timing takes about `budget_s`; the bytes counted are those rows' share
+    of the live band (its K/V rows are read once per query row)."""
+    import numpy as np
+    import oracle
+
+    oracle.build()
+    q, k, v = step.q[0].cpu(), step.k[0].cpu(), step.v[0].cpu()
+    rows_total = w.B * w.NH
+    per_row_bytes = step.live / rows_total
+
+    def timed(nrows, nthreads, reps=1):
+        want = np.zeros(rows_total, dtype=bool)
+        want[:nrows] = True
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.decode(q, k, v, step.lens_h, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale, want=want,
+                          nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    out = {}
+    for label, nthreads in (("all_cores", 0), ("one_thread", 1)):
+        threads = (os.cpu_count() or 1) if nthreads == 0 else 1
+        t1 = max(timed(1, nthreads), 1e-6)
+        nrows = max(1, min(rows_total, int(budget_s / t1) * threads))
+        reps = 1
+        if nrows == rows_total:  # the whole layer is cheap: repeat it to fill the budget
+            reps = max(1, int(budget_s / max(timed(nrows, nthreads), 1e-6)))
+        t = timed(nrows, nthreads, reps)
+        out[label] = {"GBps": per_row_bytes * nrows * reps / t / 1e9, "rows": nrows, "calls": reps,
+                      "seconds": round(t, 3)}
+    out["threads_all_cores"] = os.cpu_count() or 1
+    return out
+
+
 def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
     from decode_attention_04_gb300.inputs import draw_lens
     lens = draw_lens(w)
@@ -364,6 +401,8 @@ def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
            "us_single_call_plain_launch": time_single_calls(st, 20, stream),
            "us_l2_hot_one_layer": time_l2_hot(st, steps, stream),
            "l2_hot_fits": st.live <= L2_BYTES // 2}
+    if kv == "bf16":
+        res["cpu_oracle"] = cpu_oracle_sample(w, st)
     del st
     torch.cuda.empty_cache()
     return res
