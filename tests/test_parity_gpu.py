@@ -292,3 +292,19 @@ def test_extreme_score_scales_match_oracle(q_mul):
     ref = oracle_ref(w, q, k, v, lens)
     for path in (fd.FD_PATH_TC, fd.FD_PATH_SIMT):
         check(run(w, q, k, v, lens, path=path), ref, what=f"q x {q_mul} path {path}")
+
+
+@pytest.mark.parametrize("B", [64, 200], ids=["B64_longest_first", "B200_natural_order"])
+def test_large_batches_around_the_ordering_cutoff(B):
+    """Batches at the longest-band-first limit (64 sequences) and above it
+    (blocks in natural order), with empty sequences and lengths beyond the
+    capacity (no window: the band is clamped and flagged)."""
+    rng = np.random.default_rng(B)
+    lens = tuple(int(x) for x in rng.integers(0, 41, size=B))
+    w = W(f"batch{B}", B, 8, 8, 64, 32, 0, lens=lens, seed=49 + B)
+    q, k, v, ln = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, ln)
+    for path in (fd.FD_PATH_TC, fd.FD_PATH_SIMT):
+        res = run(w, q, k, v, ln, path=path)
+        assert res["deverr"] == (fd.FD_DEVERR_LEN_CLAMPED if max(lens) > 32 else 0)
+        check(res, ref, what=f"B={B} path {path}")
