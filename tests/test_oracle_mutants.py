@@ -113,3 +113,80 @@ def test_unmutated_source_passes_the_same_checks(tmp_path):
     lib = ctypes.CDLL(str(so))
     assert _golden_failures(lib) == 0
     assert _brute_failures(lib) == 0
+
+
+# ---------------------------------------------------------------- E4M3 form
+
+FP8_MUTANTS = {
+    "e4m3_bias_off_by_one": ("std::ldexp(1.0 + m / 8.0, e - 7)", "std::ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_subnormal_as_normal": ("e == 0 ? std::ldexp(m / 8.0, -6)", "e == 0 ? std::ldexp(1.0 + m / 8.0, -7)"),
+    "e4m3_every_top_code_nan": ("if (e == 15 && m == 7) return", "if (e == 15) return"),
+    "e4m3_sign_dropped": ("return s ? -mag : mag;", "return mag;"),
+    "v_scale_dropped": ("e4m3_to_double(p.v8[row * p.HS + d]) * vs;", "e4m3_to_double(p.v8[row * p.HS + d]);"),
+    "v_takes_k_scale": ("e4m3_to_double(p.v8[row * p.HS + d]) * vs;", "e4m3_to_double(p.v8[row * p.HS + d]) * ks;"),
+    "scale_ignores_sequence": ("const double ks = p.k_scale[static_cast<int64_t>(b) * p.NKV + kvh];",
+                               "const double ks = p.k_scale[kvh];"),
+}
+
+
+def _build(src_text: str, name: str, tmp: Path):
+    mpath = tmp / f"{name}.cpp"
+    mpath.write_text(src_text)
+    so = tmp / f"lib{name}.so"
+    subprocess.run(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(mpath), "-o", str(so)],
+                   check=True)
+    return ctypes.CDLL(str(so))
+
+
+def _fp8_failures(lib) -> int:
+    """The E4M3 pins, restated against torch: the 256-code table equals
+    torch's float8_e4m3fn conversion, and the E4M3 form equals float64 SDPA
+    over the cache dequantised by torch (per-(sequence, KV head) scales)."""
+    from decode_attention_04_gb300.inputs import make_inputs_fp8
+    fails = 0
+    table = np.zeros(256)
+    lib.fd_oracle_e4m3_table(ctypes.c_void_p(table.ctypes.data))
+    ref_table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if not (np.array_equal(np.isnan(table), np.isnan(ref_table)) and
+            np.array_equal(table[~np.isnan(ref_table)], ref_table[~np.isnan(ref_table)])):
+        fails += 1
+    for B, NH, NKV, HS, cap, win, lens in [(2, 8, 2, 64, 48, 0, (40, 23)), (2, 16, 1, 128, 32, 20, (70, 5))]:
+        w = Workload("m8", B, NH, NKV, HS, cap, win, lens=lens, seed=5)
+        q, k8, v8, ks, vs, ln = make_inputs_fp8(w)
+        out = np.zeros((B, NH, HS))
+        P = ctypes.c_void_p
+
+        def arr(t, dt):
+            return np.ascontiguousarray(t.contiguous().numpy().astype(dt, copy=False))
+        qb = np.ascontiguousarray(q.contiguous().view(torch.int16).numpy().view(np.uint16))
+        kc, vc = arr(k8, np.uint8), arr(v8, np.uint8)
+        ksa, vsa = arr(ks, np.float32), arr(vs, np.float32)
+        lna = np.ascontiguousarray(np.asarray(ln, dtype=np.int32))
+        lib.fd_oracle_decode_fp8(P(qb.ctypes.data), P(kc.ctypes.data), P(vc.ctypes.data), P(ksa.ctypes.data),
+                                 P(vsa.ctypes.data), P(lna.ctypes.data), B, NH, NKV, HS, cap, win,
+                                 ctypes.c_double(w.scale), None, 1, P(out.ctypes.data))
+        kd = k8.view(torch.float8_e4m3fn).to(torch.float64) * ks.double()[:, :, None, None]
+        vd = v8.view(torch.float8_e4m3fn).to(torch.float64) * vs.double()[:, :, None, None]
+        G = NH // NKV
+        keep = min(win if win > 0 else cap, cap)
+        for b in range(B):
+            L = int(ln[b])
+            pos = torch.arange(max(0, L - keep), L)
+            kk = kd[b][:, pos % cap].repeat_interleave(G, dim=0)
+            vv = vd[b][:, pos % cap].repeat_interleave(G, dim=0)
+            o = torch.nn.functional.scaled_dot_product_attention(q[b].double().unsqueeze(1), kk, vv, scale=w.scale)
+            if not np.allclose(out[b], o[:, 0].numpy(), rtol=0, atol=1e-12):
+                fails += 1
+    return fails
+
+
+@pytest.mark.parametrize("name", sorted(FP8_MUTANTS))
+def test_fp8_pins_catch_planted_mistake(name, tmp_path):
+    old, new = FP8_MUTANTS[name]
+    src = SRC.read_text()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    assert _fp8_failures(_build(src.replace(old, new), name, tmp_path)) > 0, f"mutant {name} passed every E4M3 pin"
+
+
+def test_unmutated_source_passes_the_e4m3_checks(tmp_path):
+    assert _fp8_failures(_build(SRC.read_text(), "clean8", tmp_path)) == 0
