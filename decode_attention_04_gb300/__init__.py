@@ -37,7 +37,8 @@ FD_PATH_UMMA = 3
 FD_KV_BF16 = 0
 FD_KV_E4M3 = 1
 
-EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_kv", "fd_plan_sms_kv", "fd_plan_override", "fd_workspace_bytes",
+EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_kv", "fd_plan_sms_kv", "fd_plan_override", "fd_plan_persistent",
+            "fd_workspace_bytes",
             "fd_decode_attn", "fd_decode_attn_ex", "fd_decode_attn_fp8", "fd_decode_attn_fp8_ex",
             "fd_decode_attn_noalloc", "fd_get_device_error", "fd_release", "fd_strerror", "fd_version"]
 
@@ -56,6 +57,7 @@ class fd_plan_t(ctypes.Structure):
         ("group_bytes", ctypes.c_int),
         ("kv_dtype", ctypes.c_int),
         ("consumer_warps", ctypes.c_int),
+        ("persistent", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("workspace_zero_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),
@@ -97,6 +99,7 @@ def load_library(path: Path | str | None = None):
         "fd_plan_kv": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_sms_kv": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_override": (ci, [planp, ci, ci, ci, ci]),
+        "fd_plan_persistent": (ci, [planp, ci]),
         "fd_workspace_bytes": (sz, [planp]),
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
@@ -187,6 +190,11 @@ def fd_plan_override(plan: fd_plan_t, num_splits: int = 0, path: int = FD_PATH_A
                      fused: int = -1) -> fd_plan_t:
     _check(load_library().fd_plan_override(ctypes.byref(plan), num_splits, path, cluster, fused),
            "fd_plan_override")
+    return plan
+
+
+def fd_plan_persistent(plan: fd_plan_t, persistent: int = 1) -> fd_plan_t:
+    _check(load_library().fd_plan_persistent(ctypes.byref(plan), persistent), "fd_plan_persistent")
     return plan
 
 

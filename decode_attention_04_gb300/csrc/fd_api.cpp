@@ -37,13 +37,19 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Partial slots per row: one per block, or one per cluster of blocks.
 int slots(const fd_plan_t& p) { return p.num_splits / (p.cluster > 0 ? p.cluster : 1); }
 
-// Workspace layout when a row has more than one partial slot:
-//   [counters: B*NKV uint32, must be zero before the first call]
-//   [O partials: fp32 B*NH*slots*HS] [(m, l): fp32 B*NH*slots*2]
+// Workspace layout:
+//   [counters: B*NKV uint32 split counters when a row has more than one
+//    partial slot, then one work-item counter for a persistent grid; zero
+//    before the first call]
+//   [O partials: fp32 B*NH*slots*HS] [(m, l): fp32 B*NH*slots*2]   (slots > 1)
 // each part rounded up to 256 bytes.
+long long split_counter_words(const fd_plan_t& p) {
+  return slots(p) > 1 ? static_cast<long long>(p.B) * p.NKV : 0;
+}
+
 size_t ws_counter_bytes(const fd_plan_t& p) {
-  if (slots(p) <= 1) return 0;
-  return round_up(static_cast<size_t>(p.B) * p.NKV * sizeof(unsigned int), 256);
+  const long long words = split_counter_words(p) + (p.persistent > 0 ? 1 : 0);
+  return words ? round_up(static_cast<size_t>(words) * sizeof(unsigned int), 256) : 0;
 }
 
 size_t ws_o_bytes(const fd_plan_t& p) {
@@ -51,9 +57,39 @@ size_t ws_o_bytes(const fd_plan_t& p) {
 }
 
 size_t ws_total(const fd_plan_t& p) {
-  if (slots(p) <= 1) return 0;
+  if (slots(p) <= 1) return ws_counter_bytes(p);
   return ws_counter_bytes(p) + ws_o_bytes(p) +
          round_up(static_cast<size_t>(p.B) * p.NH * slots(p) * 2 * sizeof(float), 256);
+}
+
+// Work items of the split grid: one per (split, KV head, sequence).
+long long work_items(const fd_plan_t& p) { return static_cast<long long>(p.num_splits) * p.NKV * p.B; }
+
+// A persistent split grid (a fixed set of blocks taking work items from a
+// device counter) is available for the tensor-core kernel without clusters
+// or the fused merge.
+bool persistent_allowed(const fd_plan_t& p) {
+  const long long items = work_items(p);
+  return p.path == FD_PATH_TC && p.cluster == 1 && !p.fused && items >= 1 && items <= (1ll << 30);
+}
+
+// Blocks of a persistent grid: every resident block slot once, or one per
+// item when there are fewer items.
+int persistent_blocks(const fd_plan_t& p) {
+  const long long slots_gpu = static_cast<long long>(p.num_sms) * p.ctas_per_sm;
+  return static_cast<int>(std::max(1ll, std::min(work_items(p), slots_gpu)));
+}
+
+// Off by default: measured on GB300 (us per layer, graph of layers, one
+// block per split -> persistent), the two multi-wave workloads barely moved
+// (ragged d128 batch 168.0 -> 167.8, or 166.7 at twice the splits; MQA long
+// 174.8 -> 172.5; E4M3 MQA long 122.9 -> 126.5) and one-wave grids lost
+// (ring 7.42 -> 9.17, llama tiny 5.84 -> 6.92): the hardware already starts a
+// new block as soon as one retires, and the persistent kernel holds more
+// registers, which keeps the merge kernel's early blocks off the SMs.
+int persistent_rule(const fd_plan_t& p) {
+  (void)p;
+  return 0;
 }
 
 // Fused merge (the last split block of each (sequence, KV head) merges) when
@@ -107,8 +143,10 @@ int warps_rule(const fd_plan_t& p) {
   return (p.HS == 256 || (p.HS == 512 && two)) ? 8 : 4;
 }
 
-void finish_plan(fd_plan_t* p, int fused = -1) {
+void finish_plan(fd_plan_t* p, int fused = -1, int persistent = -1) {
   p->fused = fused < 0 ? fused_rule(*p) : (fused && fused_rule_allowed(*p) ? 1 : 0);
+  p->persistent = persistent < 0 ? persistent_rule(*p)
+                                 : (persistent && persistent_allowed(*p) ? persistent_blocks(*p) : 0);
   p->group_bytes = group_rule(*p);
   p->consumer_warps = warps_rule(*p);
   p->workspace_bytes = ws_total(*p);
@@ -304,6 +342,8 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.lens = lens;
   char* ws = static_cast<char*>(workspace);
   a.counters = need ? reinterpret_cast<unsigned int*>(ws) : nullptr;
+  a.persistent = plan.persistent;
+  a.work_counter = plan.persistent > 0 ? a.counters + split_counter_words(plan) : nullptr;
   a.ws_o = need ? reinterpret_cast<float*>(ws + ws_counter_bytes(plan)) : nullptr;
   a.ws_ml = need ? reinterpret_cast<float*>(ws + ws_counter_bytes(plan) + ws_o_bytes(plan)) : nullptr;
   a.fused = plan.fused;
@@ -388,6 +428,22 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
   return FD_OK;
 }
 
+int fd_plan_persistent(fd_plan_t* plan, int persistent) {
+  if (!plan || persistent < -1 || persistent > 1) return FD_ERR_INVALID_ARG;
+  if (check_shape(plan->B, plan->NH, plan->NKV, plan->HS, plan->capacity, plan->window) != FD_OK)
+    return FD_ERR_INVALID_ARG;
+  fd_plan_t p = *plan;
+  if (p.num_splits < 1 || !valid_path(p) || !valid_kv(p.kv_dtype, p.path) ||
+      !valid_cluster(p.cluster, p.num_splits, p.HS, p.path) || p.num_sms < 1 || p.ctas_per_sm < 1)
+    return FD_ERR_INVALID_ARG;
+  if (persistent == 1 && !persistent_allowed(p)) return FD_ERR_INVALID_ARG;
+  finish_plan(&p, p.fused, persistent);
+  p.consumer_warps = plan->consumer_warps;  // a forced warp count stays
+  p.group_bytes = plan->group_bytes;
+  *plan = p;
+  return FD_OK;
+}
+
 size_t fd_workspace_bytes(const fd_plan_t* plan) { return plan ? ws_total(*plan) : 0; }
 
 }  // extern "C"
@@ -405,6 +461,9 @@ int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int 
     return FD_ERR_INVALID_ARG;
   if (plan->num_splits < 1 || !valid_path(*plan) || plan->granule < 1 || !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
       (plan->fused && !fused_rule_allowed(*plan)))
+    return FD_ERR_INVALID_ARG;
+  if (plan->persistent < 0 ||
+      (plan->persistent > 0 && (!persistent_allowed(*plan) || plan->persistent > work_items(*plan))))
     return FD_ERR_INVALID_ARG;
   if (plan->consumer_warps != warps_rule(*plan) &&
       !(warps_choice_open(*plan) && (plan->consumer_warps == 4 || plan->consumer_warps == 8)))

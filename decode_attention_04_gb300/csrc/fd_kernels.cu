@@ -288,14 +288,18 @@ struct TcCfg {
 };
 
 constexpr int kLptMaxB = 64;
+constexpr int kItemQ = 4;  // work items a persistent block's roles may be apart
 
-// The sequence that blocks with blockIdx.z == z work on: the z-th longest band
-// (ties by index) when 1 < B <= kLptMaxB, else z itself. Blocks start in
-// blockIdx order, so the longest splits start first and the last wave holds
-// the short ones (longest-processing-time-first order); every order gives the
-// same partials. Every thread of the block calls it (it synchronises).
-__device__ int lpt_sequence(const LaunchArgs& a, int z, int tid, int nthreads, int* s_seq) {
-  if (a.B <= 1 || a.B > kLptMaxB) return z;
+// Order in which the split blocks (or a persistent grid's work items) visit
+// the sequences: s_seq[z] = the z-th longest band (ties by index) when
+// 1 < B <= kLptMaxB, else the identity (s_seq unused). Blocks start in
+// blockIdx order and work items are taken in index order, so the longest
+// splits start first and the last wave holds the short ones
+// (longest-processing-time-first order); every order gives the same partials.
+__device__ __forceinline__ bool lpt_ordered(const LaunchArgs& a) { return a.B > 1 && a.B <= kLptMaxB; }
+
+__device__ void lpt_table(const LaunchArgs& a, int tid, int nthreads, int* s_seq) {
+  if (!lpt_ordered(a)) return;
   int lo;
   for (int t = tid; t < a.B; t += nthreads) {
     const int bt = band_of(a.lens[t], a.capacity, a.window, false, &lo);
@@ -306,18 +310,16 @@ __device__ int lpt_sequence(const LaunchArgs& a, int z, int tid, int nthreads, i
     }
     s_seq[rank] = t;
   }
-  __syncthreads();
-  return s_seq[z];
 }
 
-template <class C>
+template <class C, bool PERSIST = false>
 __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_seq[kLptMaxB];
-  const int s = blockIdx.x, kvh = blockIdx.y;
+  __shared__ int s_item[kItemQ];
+  __shared__ __align__(8) uint64_t s_ibar[2 * kItemQ];  // work item queue: full[], empty[]
   const int G = a.NH / a.NKV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hbase = kvh * G;
 
   float* sS = reinterpret_cast<float*>(smem + C::OFF_S);
   uint16_t* sP = reinterpret_cast<uint16_t*>(smem + C::OFF_P);
@@ -333,6 +335,10 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       mbar_init(full0 + 8 * i, 64);         // every lane of both producer warps arrives once per phase
       mbar_init(empty0 + 8 * i, C::NWC);    // one arrival per consumer warp
     }
+    for (int i = 0; i < kItemQ; ++i) {
+      mbar_init(smem_u32(s_ibar + i), 1);                   // the K producer publishes
+      mbar_init(smem_u32(s_ibar + kItemQ + i), C::NWC + 1);  // consumer warps and the V producer took it
+    }
     fence_mbar_init();
   }
   // Start P at zero and alpha at 1 so nothing read before its first write can
@@ -345,7 +351,53 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   grid_dependency_wait();
   grid_launch_dependents();
-  const int b = lpt_sequence(a, blockIdx.z, tid, C::THREADS, s_seq);
+  lpt_table(a, tid, C::THREADS, s_seq);
+  __syncthreads();
+
+  // One work item (sequence, KV head, split) per block, or with a persistent
+  // grid a stream of them: the K producer's lane 0 takes the next item index
+  // from the counter and publishes it in a small shared-memory queue; the V
+  // producer and the consumers read it from there. The counter wraps to zero
+  // as the last block takes its final (past-the-end) index, so it is zero
+  // again for the next call. Producers run ahead into the next item while the
+  // consumers finish the current one: the stage ring and its phases continue
+  // across items (gbase counts the tiles of earlier items).
+  constexpr bool persist = PERSIST;  // a separate instantiation: the per-split grid keeps its registers
+  const int n_items = persist ? a.num_splits * a.NKV * a.B : 1;
+  bool failed = false;
+  int gnext = 0;
+  for (int it = 0;; ++it) {
+  int s, kvh, z;
+  if (!persist) {
+    if (it > 0) break;
+    s = blockIdx.x;
+    kvh = blockIdx.y;
+    z = blockIdx.z;
+  } else {
+    const int qi = it % kItemQ;
+    const uint32_t ifull = smem_u32(s_ibar + qi), iempty = smem_u32(s_ibar + kItemQ + qi);
+    int w = 0;
+    if (warp == C::NWC) {
+      if (lane == 0) {
+        // take an index even after a failed wait, so the counter still wraps
+        if (it >= kItemQ) mbar_wait(iempty, ((it / kItemQ) - 1) & 1, failed);
+        w = static_cast<int>(atomicInc(a.work_counter, static_cast<unsigned>(n_items + gridDim.x - 1)));
+        s_item[qi] = w;
+        mbar_arrive(ifull);
+      }
+      w = __shfl_sync(0xffffffffu, w, 0);
+    } else {
+      w = mbar_wait(ifull, (it / kItemQ) & 1, failed) ? s_item[qi] : n_items;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(iempty);
+    }
+    if (w >= n_items) break;
+    s = w % a.num_splits;
+    kvh = (w / a.num_splits) % a.NKV;
+    z = w / (a.num_splits * a.NKV);
+  }
+  const int b = lpt_ordered(a) ? s_seq[z] : z;
+  const int hbase = kvh * G;
 
   int lo;
   const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
@@ -366,12 +418,13 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         if (a.out_f32) a.out_f32[o] = 0.f;
       }
     }
-    return;
+    continue;
   }
   // In a cluster every block, even one with an empty slice (m = -inf, l = 0,
   // O = 0), takes part in the reduction at the end.
   const int ntiles = (n + C::T - 1) / C::T;
-  __syncthreads();
+  const int gbase = gnext;  // pipeline tiles of this block's earlier items
+  gnext += ntiles;
 
   const int grp = lane >> 2, t4 = lane & 3;
   const int dbase = warp * C::DW;
@@ -399,10 +452,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     constexpr int kGroupPitch = C::KV8 ? C::GP8 : C::GP;
     constexpr size_t kStageBytes = C::KV8 ? C::STAGE8_BYTES : C::STAGE_BYTES;
     const size_t ring = C::KV8 ? (is_k ? C::OFF_K8 : C::OFF_V8) : (is_k ? C::OFF_K : C::OFF_V);
-    bool failed = false;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i % C::NSTAGE;
-      if (i >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((i / C::NSTAGE) - 1) & 1, failed);
+      const int gi = gbase + i;
+      const int st = gi % C::NSTAGE;
+      if (gi >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((gi / C::NSTAGE) - 1) & 1, failed);
+      if (persist && failed) continue;  // nothing waits for these copies any more
       const int nv = min(C::T, n - i * C::T);
       const long long pbase = p0 + static_cast<long long>(i) * C::T;
       const uint32_t dst = smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes);
@@ -490,11 +544,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 
   // ldmatrix lane addressing
   const int lrow = lane & 7, lmat = lane >> 3;
-  bool failed = false;
 
   for (int i = 0; i < ntiles; ++i) {
-    const int st = i % C::NSTAGE;
-    mbar_wait(full0 + 8 * st, (i / C::NSTAGE) & 1, failed);
+    const int gi = gbase + i;
+    const int st = gi % C::NSTAGE;
+    mbar_wait(full0 + 8 * st, (gi / C::NSTAGE) & 1, failed);
     const int nv = min(C::T, n - i * C::T);  // valid tile positions: [0, nv)
     const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES;
     unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
@@ -719,7 +773,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   if (CS == 1) {
     // ---- one block per slice: its partial (O, m, l), or with one split the
     // normalised row
-    if (warp >= C::NWC) return;
+    if (warp >= C::NWC) continue;
 #pragma unroll
     for (int mt = 0; mt < C::KD; ++mt)
 #pragma unroll
@@ -743,7 +797,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       a.ws_ml[r] = sM[tid];
       a.ws_ml[r + 1] = sL[tid];
     }
-    if (direct || !a.fused) return;
+    if (direct || !a.fused) continue;
 
     // ---- fused merge: the last block of this (sequence, KV head) to finish
     // combines every partial of the group (no merge launch). The counter
@@ -931,6 +985,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     a.ws_ml[r + 1] = sLt[tid];
   }
   cluster_sync_all();  // no block leaves while another still reads its shared memory
+  }  // work items
 }
 
 // ================================================================ merge kernel
@@ -1053,6 +1108,12 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
   if (a.cluster > 8) {
     e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+  }
+  if (a.persistent > 0) {
+    e = cudaFuncSetAttribute(split_tc_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(split_tc_kernel<C, true>, dim3(a.persistent), dim3(C::THREADS), C::SMEM, stream, 1, a);
   }
   dim3 grid(a.num_splits, a.NKV, a.B);
   return launch_pdl(split_tc_kernel<C>, grid, dim3(C::THREADS), C::SMEM, stream, a.cluster, a);

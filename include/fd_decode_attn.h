@@ -159,6 +159,7 @@ typedef struct {
   int group_bytes;         /* bytes per bulk-copy group of a tile: 2048 or 4096 (bf16); 2048 or 1024 (E4M3) */
   int kv_dtype;            /* FD_KV_BF16 or FD_KV_E4M3: the cache type the plan was made for */
   int consumer_warps;      /* MMA warps per split block (2, 4 or 8; 0 on the SIMT path) */
+  int persistent;          /* blocks of a persistent split grid (fd_plan_persistent); 0: one block per split */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
   size_t workspace_zero_bytes; /* leading workspace bytes that must be zero before first use */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
@@ -213,13 +214,37 @@ int fd_plan_sms_kv(int B, int NH, int NKV, int HS, int capacity, int window, int
 int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int fused);
 
 /*
+ * fd_plan_persistent: run the split kernel as a persistent grid (persistent =
+ * 1), as one block per split (0), or as the plan's rule decides (-1).
+ * "Hand-Writing Gemma 4 Flash-Decoding + an FP4 Matvec Bonus (Part 2)",
+ * section "One KV head breaks the textbook", gives each (KV head, split) its
+ * own block; a persistent grid keeps one block per resident block slot
+ * (plan->persistent = min(work items, num_sms * ctas_per_sm)) and hands out the
+ * work items (split, KV head, sequence), longest bands first as in the
+ * one-block-per-split order, from a 32-bit counter in the workspace. A block's
+ * copy warps stream the next item's first tiles while its MMA warps finish the
+ * current one, so the pipeline does not drain and refill between items. The
+ * counter wraps back to zero when the last block takes its final index, so the
+ * workspace stays reusable. Tensor-core path only, without clusters or the
+ * fused merge; fd_plan_override resets the choice to the plan's rule, and
+ * plans use persistent = 0 (on GB300 it gained at most ~1% on multi-wave
+ * grids and lost on one-wave grids). The result is bit-identical to one
+ * block per split (the same partials, merged in the same order).
+ * Errors: FD_ERR_INVALID_ARG (bad plan or mode, or persistent = 1 where it is
+ * not available).
+ */
+int fd_plan_persistent(fd_plan_t* plan, int persistent);
+
+/*
  * fd_workspace_bytes: workspace a plan needs. With P = num_splits / cluster
- * partial slots per row and P > 1: B * NKV 32-bit split counters, then
- * B * NH * P * HS fp32 partial outputs, then B * NH * P * 2 fp32 (m, l), each
- * part rounded up to 256 bytes. 0 when P == 1 (the split kernel then writes
- * the output itself). The counters (the first workspace_zero_bytes bytes)
- * must be zero before a workspace's first use; every completed call leaves
- * them zero.
+ * partial slots per row: when P > 1, B * NKV 32-bit split counters; with a
+ * persistent grid, one more 32-bit work-item counter; when P > 1, then
+ * B * NH * P * HS fp32 partial outputs and B * NH * P * 2 fp32 (m, l). Each
+ * part is rounded up to 256 bytes. 0 when P == 1 without a persistent grid
+ * (the split kernel then writes the output itself). The counters (the first
+ * workspace_zero_bytes bytes) must be zero before a workspace's first use;
+ * every completed call leaves them zero (after a call that reported
+ * FD_DEVERR_WAIT_TIMEOUT, clear them again).
  */
 size_t fd_workspace_bytes(const fd_plan_t* plan);
 

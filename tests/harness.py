@@ -44,9 +44,10 @@ class Guarded:
 
 def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len: int = 0,
         poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None, cluster: int = 0,
-        fused: int = -1):
+        fused: int = -1, persistent: int = -1):
     """One fd_decode_attn_ex call. Returns dict with out (bf16, cpu), out32
-    (fp32, cpu), plan, deverr, canaries (bool)."""
+    (fp32, cpu), plan, deverr, canaries (bool). persistent: -1 the plan's
+    rule, 0 one block per split, k > 0 a persistent grid of at most k blocks."""
     dev = torch.device(device)
     if inputs_on_device:
         qd, kd, vd, ld = q, k, v, lens.to(dev)
@@ -55,6 +56,7 @@ def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len:
     plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len)
     if splits or path or cluster or fused >= 0:
         fd.fd_plan_override(plan, splits, path, cluster, fused)
+    set_persistent(plan, persistent)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)         # NaN-filled: unwritten rows show up
     o32 = Guarded(n * 4, dev, fill=0xFF)
@@ -72,6 +74,16 @@ def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len:
                 out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(),
                 plan=plan, deverr=err, counters_zero=counters_zero,
                 canaries=o16.canaries_intact() and o32.canaries_intact() and ws.canaries_intact())
+
+
+def set_persistent(plan, persistent: int):
+    """-1: leave the plan's choice; 0: one block per split; k > 0: a persistent
+    grid, narrowed to k blocks when the plan's grid is larger."""
+    if persistent < 0:
+        return
+    fd.fd_plan_persistent(plan, 1 if persistent else 0)
+    if 0 < persistent < plan.persistent:
+        plan.persistent = persistent
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
@@ -112,7 +124,7 @@ def oracle_ref(w, q, k, v, lens, rows=None):
 
 
 def run_fp8(w, q, k8, v8, ks, vs, lens, splits: int = 0, max_len: int = 0, device="cuda",
-            inputs_on_device=False, scale=None, cluster: int = 0, fused: int = -1):
+            inputs_on_device=False, scale=None, cluster: int = 0, fused: int = -1, persistent: int = -1):
     """One fd_decode_attn_fp8_ex call over an E4M3 cache (codes k8/v8, scales
     ks/vs); same result dict as run()."""
     dev = torch.device(device)
@@ -123,6 +135,7 @@ def run_fp8(w, q, k8, v8, ks, vs, lens, splits: int = 0, max_len: int = 0, devic
     plan = fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, max_len, kv_dtype=fd.FD_KV_E4M3)
     if splits or cluster or fused >= 0:
         fd.fd_plan_override(plan, splits, 0, cluster, fused)
+    set_persistent(plan, persistent)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)
     o32 = Guarded(n * 4, dev, fill=0xFF)

@@ -296,3 +296,66 @@ def test_tcgen05_family_is_opt_in_and_shape_bound(lib):
         q = fd.fd_plan_t.from_buffer_copy(p)
         with pytest.raises(fd.FdError):
             fd.fd_plan_override(q, *bad)
+
+
+def test_persistent_grid_is_opt_in_and_sized(lib):
+    """fd_plan_persistent: one block per resident slot (or per item), one more
+    zeroed counter word in the workspace, tensor-core path without clusters or
+    the fused merge only; fd_plan_override returns to the plan's rule."""
+    up = lambda x: -(-x // 256) * 256
+    for name in WORKLOADS:
+        assert _plan(WORKLOADS[name]).persistent == 0
+    w = WORKLOADS["llama_ragged"]
+    p = _plan(w)
+    items = p.num_splits * w.NKV * w.B
+    q = fd.fd_plan_t.from_buffer_copy(p)
+    fd.fd_plan_persistent(q, 1)
+    assert q.persistent == min(items, 152 * 2)
+    assert q.workspace_zero_bytes == up((w.B * w.NKV + 1) * 4)
+    assert q.workspace_bytes == p.workspace_bytes - p.workspace_zero_bytes + q.workspace_zero_bytes
+    assert q.workspace_bytes == fd.fd_workspace_bytes(q)
+    assert (q.num_splits, q.group_bytes, q.consumer_warps) == (p.num_splits, p.group_bytes, p.consumer_warps)
+    fd.fd_plan_persistent(q, 0)
+    assert q.persistent == 0 and q.workspace_bytes == p.workspace_bytes
+    # fewer items than block slots: one block per item; S = 1 still needs the counter
+    t = WORKLOADS["llama_tiny"]
+    s1 = _plan(t)
+    fd.fd_plan_override(s1, 1)
+    assert s1.workspace_bytes == 0
+    fd.fd_plan_persistent(s1, 1)
+    assert s1.persistent == t.B * t.NKV and s1.workspace_bytes == s1.workspace_zero_bytes == 256
+    fd.fd_plan_override(s1, 2)
+    assert s1.persistent == 0  # back to the plan's rule
+    # not available: SIMT path, clusters, fused merge; bad modes
+    for args in [(0, fd.FD_PATH_SIMT, 0, -1), (32, fd.FD_PATH_TC, 2, -1), (0, 0, 0, 1)]:
+        r = _plan(WORKLOADS["gemma_local_ring"])
+        fd.fd_plan_override(r, *args)
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_persistent(r, 1)
+        fd.fd_plan_persistent(r, 0)
+        fd.fd_plan_persistent(r, -1)
+        assert r.persistent == 0
+    for mode in (2, -2):
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_persistent(fd.fd_plan_t.from_buffer_copy(p), mode)
+
+
+def test_persistent_plan_checked_before_any_cuda_call(lib):
+    """A persistent plan with a block count outside [1, items], or one whose
+    path cannot run it, is refused by fd_decode_attn_ex before any launch."""
+    w = WORKLOADS["llama_tiny"]
+    p = _plan(w)
+    fd.fd_plan_persistent(p, 1)
+    items = p.num_splits * w.NKV * w.B
+    dummy = ctypes.c_void_p(256)  # never dereferenced: the plan check comes first
+    for bad in (-1, items + 1):
+        q = fd.fd_plan_t.from_buffer_copy(p)
+        q.persistent = bad
+        rc = lib.fd_decode_attn_ex(ctypes.byref(q), dummy, q.workspace_bytes, None, dummy, dummy, dummy, dummy,
+                                   dummy, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
+        assert rc == fd.FD_ERR_INVALID_ARG
+    q = fd.fd_plan_t.from_buffer_copy(p)
+    q.path, q.consumer_warps = fd.FD_PATH_SIMT, 0  # a valid SIMT plan but for the persistent grid
+    rc = lib.fd_decode_attn_ex(ctypes.byref(q), dummy, q.workspace_bytes, None, dummy, dummy, dummy, dummy,
+                               dummy, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
+    assert rc == fd.FD_ERR_INVALID_ARG
