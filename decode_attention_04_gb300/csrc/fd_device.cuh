@@ -49,6 +49,24 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
+// The partial of a split whose slice of the band is empty: O = 0, m = -inf,
+// l = 0, which has weight 0 in the merge. Every split block writes one, so the
+// merge kernel reads all S partial slots of a row without first reading the
+// row's length. G rows of HS floats at slot s of S; HS % 4 == 0.
+__device__ __forceinline__ void write_empty_partial(const LaunchArgs& a, int b, int hbase, int G, int HS, int s,
+                                                    int tid, int nthreads) {
+  const int S = a.num_splits;
+  const int hs4 = HS / 4;
+  for (int i = tid; i < G * hs4; i += nthreads) {
+    const size_t row = static_cast<size_t>(b) * a.NH + hbase + i / hs4;
+    reinterpret_cast<float4*>(a.ws_o + (row * S + s) * HS)[i % hs4] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int g = tid; g < G; g += nthreads) {
+    const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
+    reinterpret_cast<float2*>(a.ws_ml)[row * S + s] = make_float2(kNegInf, 0.f);
+  }
+}
+
 // ------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <algorithm>
 #include <cstdint>
 #include <utility>
 
@@ -124,6 +125,8 @@ __global__ void __launch_bounds__(kSimtThreads) split_simt_kernel(const LaunchAr
         a.out[o] = 0;
         if (a.out_f32) a.out_f32[o] = 0.f;
       }
+    } else {
+      write_empty_partial(a, b, hbase, G, HS, s, tid, kSimtThreads);
     }
     return;
   }
@@ -351,6 +354,10 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   grid_dependency_wait();
   grid_launch_dependents();
+  // A per-split block whose sequence needs no ordering table reads its length
+  // before the barrier, so the load's latency overlaps the barrier wait.
+  const bool len_early = !PERSIST && !lpt_ordered(a);
+  const int len_first = len_early ? a.lens[blockIdx.z] : 0;
   lpt_table(a, tid, C::THREADS, s_seq);
   __syncthreads();
 
@@ -400,7 +407,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int hbase = kvh * G;
 
   int lo;
-  const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
+  const int band = band_of(len_early ? len_first : a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0,
+                           &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
   const long long p0 = lo + static_cast<long long>(s) * chunk;
   const long long p1 = min(static_cast<long long>(lo) + band, p0 + chunk);
@@ -417,6 +425,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
         a.out[o] = 0;
         if (a.out_f32) a.out_f32[o] = 0.f;
       }
+    } else if (!a.fused) {
+      write_empty_partial(a, b, hbase, G, C::HS, s, tid, C::THREADS);
     }
     continue;
   }
@@ -991,12 +1001,18 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 // ================================================================ merge kernel
 
 constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 8;  // splits whose loads one warp issues together
+constexpr int kMergeBatch = 8;        // partials whose loads one warp issues together
+constexpr int kMergeStagedRows = 64;  // rows (B * NH) from which the staged merge is used
 
-// One block per (32-dim slab, query head, sequence). Lane = dim in the slab,
-// warp w = partials w, w + 8, ...; M = max_s m_s, w_s = 2^(m_s - M),
-// out = sum_s w_s O_s / sum_s w_s l_s. Each warp issues the loads of
-// kMergeBatch partials before using any of them.
+// The merge for few rows (B * NH < kMergeStagedRows), where it is one short
+// step in a chain of launches. One block per (32-dim slab, query head,
+// sequence); lane = dim in the slab, warp w = partial slots w, w + 8, ...;
+// each warp issues the loads of kMergeBatch partials before using any and
+// folds them into a running (max, sum, O); the eight warp results are then
+// combined the same way: M = max_s m_s, w_s = 2^(m_s - M),
+// out = sum_s w_s O_s / sum_s w_s l_s. The first batch of loads goes out
+// with the load of the row's length (every slot is in bounds); slots past
+// the row's active splits are masked once the length has arrived.
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
   __shared__ float sacc[kMergeWarps][32];
   __shared__ float sl[kMergeWarps];
@@ -1005,30 +1021,42 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dependency_wait();
   grid_launch_dependents();
-  int lo;
-  const int band = band_of(a.lens[b], a.capacity, a.window, false, &lo);
-  const int chunk = chunk_of(band, a.num_splits, a.granule);
-  // one partial per block (cluster size 1) or per cluster of CS blocks
+  const int len_b = a.lens[b];
   const int CS = a.cluster;
-  const int nslots = a.num_splits / CS;
-  const int ns = (active_splits(band, chunk) + CS - 1) / CS;
+  const int nslots = a.num_splits / CS;  // one partial per block, or per cluster of blocks
   const size_t row = static_cast<size_t>(b) * a.NH + h;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml + row * nslots * 2);
   const int d = slab * 32 + lane;
-
-  // Each warp folds its splits into a running (max, sum, O) with one rescale
-  // per batch, so the whole row costs one memory round trip per batch; the
-  // eight warp results are then combined the same way.
-  float mw = kNegInf, lw = 0.f, acc = 0.f;
   const float* ob = a.ws_o + row * nslots * a.HS + d;
-  for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeBatch) {
-    float2 mlv[kMergeBatch];
-    float ov[kMergeBatch];
+  float2 mlv[kMergeBatch];
+  float ov[kMergeBatch];
 #pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-      const int s = s0 + kMergeWarps * u;
-      mlv[u] = s < ns ? ml[s] : make_float2(kNegInf, 0.f);
-      ov[u] = s < ns ? ob[static_cast<size_t>(s) * a.HS] : 0.f;
+  for (int u = 0; u < kMergeBatch; ++u) {
+    const int s = warp + kMergeWarps * u;
+    mlv[u] = s < nslots ? ml[s] : make_float2(kNegInf, 0.f);
+    ov[u] = s < nslots ? ob[static_cast<size_t>(s) * a.HS] : 0.f;
+  }
+  int lo;
+  const int band = band_of(len_b, a.capacity, a.window, false, &lo);
+  const int chunk = chunk_of(band, a.num_splits, a.granule);
+  const int ns = (active_splits(band, chunk) + CS - 1) / CS;
+  float mw = kNegInf, lw = 0.f, acc = 0.f;
+  for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeBatch) {
+    if (s0 != warp) {
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const int s = s0 + kMergeWarps * u;
+        mlv[u] = s < ns ? ml[s] : make_float2(kNegInf, 0.f);
+        ov[u] = s < ns ? ob[static_cast<size_t>(s) * a.HS] : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        if (s0 + kMergeWarps * u >= ns) {
+          mlv[u] = make_float2(kNegInf, 0.f);
+          ov[u] = 0.f;
+        }
+      }
     }
     float bm = kNegInf;
 #pragma unroll
@@ -1068,6 +1096,117 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
     const float val = ns > 0 ? t / L : 0.f;
     a.out[row * a.HS + d] = f32_to_bf16_bits(val);
     if (a.out_f32) a.out_f32[row * a.HS + d] = val;
+  }
+}
+
+constexpr int kMergeDims = 64;        // head dims per merge block (one per thread, two threads per dim)
+constexpr int kMergeThreads = 128;
+constexpr int kMergeStageMax = 256;   // partial slots staged in shared memory at once
+
+// Shared memory of a merge block: up to kMergeStageMax slots of 64 fp32 dims.
+inline size_t merge_smem_bytes(int slots) {
+  return static_cast<size_t>(std::min(slots, kMergeStageMax)) * kMergeDims * sizeof(float);
+}
+
+// Block-wide reductions of the merge block (every thread gets the result).
+__device__ __forceinline__ float merge_block_max(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeThreads / 32; ++w) r = fmaxf(r, red[w]);
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ float merge_block_sum(float v, float* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeThreads / 32; ++w) r += red[w];  // fixed order
+  __syncthreads();
+  return r;
+}
+
+// The merge for many rows (B * NH >= kMergeStagedRows).
+// One block per (64-dim chunk, query head, sequence). Every one of the row's
+// S / cluster slots holds a partial (a split with an empty slice writes
+// O = 0, m = -inf, l = 0), so the merge needs no length. Per stage of up to
+// kMergeStageMax slots, one bulk copy per slot brings the slot's 64 dims of
+// O into shared memory while the threads load the slots' (m, l):
+// M = max_s m_s, w_s = 2^(m_s - M), L = sum_s w_s l_s; then each thread sums
+// w_s O_s over half of the slots for its dim, and out = sum / L. Stages
+// combine online (rescaled by 2^(M_old - M_new)), so one memory round trip
+// serves up to 256 partials. A row whose partials are all empty (len == 0)
+// is 0; a NaN in any m or l makes the row NaN; a NaN in O reaches its dim.
+__global__ void __launch_bounds__(kMergeThreads) merge_staged_kernel(const LaunchArgs a) {
+  extern __shared__ __align__(128) float sO[];  // [stage][kMergeDims]
+  __shared__ float sW[kMergeStageMax];
+  __shared__ float sRed[kMergeThreads / 32];
+  __shared__ float sHalf[kMergeDims];
+  __shared__ __align__(8) uint64_t bar;
+  const int tid = threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z, d0 = blockIdx.x * kMergeDims;
+  const uint32_t bar_a = smem_u32(&bar);
+  if (tid == 0) {
+    mbar_init(bar_a, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int ns = a.num_splits / a.cluster;  // one partial per block, or per cluster of blocks
+  const size_t row = static_cast<size_t>(b) * a.NH + h;
+  const float* src = a.ws_o + row * ns * a.HS + d0;
+  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row * ns;
+  const int dim = tid % kMergeDims, half = tid / kMergeDims;
+
+  float M = kNegInf, L = 0.f, acc = 0.f;
+  bool nan_ml = false, failed = false;
+  for (int base = 0, stage = 0; base < ns; base += kMergeStageMax, ++stage) {
+    const int cnt = min(kMergeStageMax, ns - base);
+    if (tid == 0) mbar_arrive_expect_tx(bar_a, static_cast<uint32_t>(cnt) * kMergeDims * 4);
+    for (int s = tid; s < cnt; s += kMergeThreads)
+      bulk_g2s(smem_u32(sO + s * kMergeDims), src + static_cast<size_t>(base + s) * a.HS, kMergeDims * 4, bar_a);
+    // this stage's (m, l): two slots per thread
+    float2 v[kMergeStageMax / kMergeThreads];
+    float mx = kNegInf;
+#pragma unroll
+    for (int k = 0; k < kMergeStageMax / kMergeThreads; ++k) {
+      const int s = tid + k * kMergeThreads;
+      v[k] = s < cnt ? ml[base + s] : make_float2(kNegInf, 0.f);
+      nan_ml |= isnan(v[k].x) || isnan(v[k].y);
+      mx = fmaxf(mx, v[k].x);
+    }
+    const float Mn = fmaxf(M, merge_block_max(mx, sRed));
+    float ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMergeStageMax / kMergeThreads; ++k) {
+      const int s = tid + k * kMergeThreads;
+      const float w = Mn == kNegInf ? 0.f : exp2f(v[k].x - Mn);  // 0 for empty partials
+      if (s < cnt) sW[s] = w;
+      ls += w * v[k].y;
+    }
+    const float sc = M == kNegInf ? 0.f : exp2f(M - Mn);  // rescales the earlier stages
+    L = L * sc + merge_block_sum(ls, sRed);               // (its barriers also publish sW)
+    acc *= sc;
+    M = Mn;
+    mbar_wait(bar_a, stage & 1, failed);
+    for (int s = half; s < cnt; s += 2) acc += sW[s] * sO[s * kMergeDims + dim];
+    __syncthreads();  // the stage's buffers are free before the next copies
+  }
+  if (half == 1) sHalf[dim] = acc;
+  const bool any_nan = __syncthreads_or(nan_ml) != 0;
+  if (half == 0) {
+    acc += sHalf[dim];
+    const float val = any_nan ? __int_as_float(0x7fc00000) : (M == kNegInf ? 0.f : acc / L);
+    a.out[row * a.HS + d0 + dim] = f32_to_bf16_bits(val);
+    if (a.out_f32) a.out_f32[row * a.HS + d0 + dim] = val;
   }
 }
 
@@ -1279,8 +1418,16 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
   // the split kernel wrote the output itself: one block / cluster per band, or
   // the fused merge by each group's last block
   if (e != cudaSuccess || a.num_splits == a.cluster || a.fused) return e;
-  dim3 mgrid(a.HS / 32, a.NH, a.B);
-  return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+  if (static_cast<long long>(a.B) * a.NH < kMergeStagedRows) {
+    dim3 mgrid(a.HS / 32, a.NH, a.B);
+    return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+  }
+  const size_t msmem = merge_smem_bytes(a.num_splits / a.cluster);
+  e = cudaFuncSetAttribute(merge_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(msmem));
+  if (e != cudaSuccess) return e;
+  dim3 mgrid(a.HS / kMergeDims, a.NH, a.B);
+  return launch_pdl(merge_staged_kernel, mgrid, dim3(kMergeThreads), msmem, stream, 1, a);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err) {

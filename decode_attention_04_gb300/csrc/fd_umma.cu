@@ -292,13 +292,15 @@ __global__ void __launch_bounds__(um::THREADS, 1)
   const long long q1 = min(static_cast<long long>(band), q0 + chunk);
   const int n = q0 < q1 ? static_cast<int>(q1 - q0) : 0;
   const bool direct = a.num_splits == 1;
-  if (n == 0) {  // len == 0 with one split: the output row is zero (no TMEM was taken)
-    if (direct) {
+  if (n == 0) {  // an empty slice (no TMEM was taken)
+    if (direct) {  // len == 0 with one split: the output row is zero
       for (int i = tid; i < G * HS; i += THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / HS) * HS + i % HS;
         a.out[o] = 0;
         if (a.out_f32) a.out_f32[o] = 0.f;
       }
+    } else {
+      write_empty_partial(a, b, hbase, G, HS, s, tid, THREADS);
     }
     return;
   }

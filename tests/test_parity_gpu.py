@@ -308,3 +308,31 @@ def test_large_batches_around_the_ordering_cutoff(B):
         res = run(w, q, k, v, ln, path=path)
         assert res["deverr"] == (fd.FD_DEVERR_LEN_CLAMPED if max(lens) > 32 else 0)
         check(res, ref, what=f"B={B} path {path}")
+
+
+@pytest.mark.parametrize("splits", [2, 257, 600])
+def test_staged_merge_with_many_partials(splits):
+    """64 or more rows (B * NH) take the staged merge (partials brought into
+    shared memory 256 slots per stage): one, two and three stages, an empty
+    sequence (all partials empty: zero rows) and sequences shorter than the
+    split count (empty partials past their active splits)."""
+    w = W("staged_merge", 4, 16, 2, 128, 1200, 0, lens=(1200, 700, 0, 5), seed=91)
+    assert w.B * w.NH >= 64
+    q, k, v, lens = make_inputs(w)
+    res = run(w, q, k, v, lens, splits=splits)
+    assert res["plan"].num_splits == splits and res["deverr"] == 0
+    check(res, oracle_ref(w, q, k, v, lens), what=f"S={splits}")
+    assert torch.equal(res["out32"][2], torch.zeros_like(res["out32"][2]))
+
+
+def test_staged_merge_nan_in_scores_reaches_only_its_group():
+    """A NaN key makes every row of its group NaN through the partials' m and
+    l; the other group and the other sequences stay finite (staged merge)."""
+    w = W("staged_nan", 4, 16, 2, 128, 300, 0, lens=(300, 200, 1, 77), seed=92)
+    q, k, v, lens = make_inputs(w)
+    k[1, 1, 150, 3] = float("nan")
+    res = run(w, q, k, v, lens, splits=9)
+    G = w.NH // w.NKV
+    out = res["out32"]
+    assert torch.isnan(out[1, G:]).all()
+    assert torch.isfinite(out[1, :G]).all() and torch.isfinite(out[[0, 2, 3]]).all()
