@@ -315,6 +315,48 @@ __device__ void lpt_table(const LaunchArgs& a, int tid, int nthreads, int* s_seq
   }
 }
 
+// Source bytes of one producer warp's tensor (K for the first producer warp,
+// V for the second) for (sequence b, KV head kvh), and its stage ring offset.
+template <class C>
+__device__ __forceinline__ const unsigned char* producer_src(const LaunchArgs& a, bool is_k, int b, int kvh) {
+  const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
+  return C::KV8 ? (is_k ? a.k8 : a.v8) + head_row0 * C::HS
+                : reinterpret_cast<const unsigned char*>((is_k ? a.k : a.v) + head_row0 * C::HS);
+}
+
+template <class C>
+__device__ __forceinline__ size_t producer_ring(bool is_k) {
+  return C::KV8 ? (is_k ? C::OFF_K8 : C::OFF_V8) : (is_k ? C::OFF_K : C::OFF_V);
+}
+
+// The bulk copies of one pipeline tile of one tensor: positions
+// [pbase, pbase + nv) (slot = position mod capacity) into stage st; lane g
+// copies group g (rows [g*R, g*R + rows) of the tile) and every lane arrives
+// on the stage's full barrier with the bytes it copies.
+template <class C>
+__device__ __forceinline__ void produce_tile(const LaunchArgs& a, const unsigned char* src, uint32_t stage_dst,
+                                             uint32_t fb, long long pbase, int nv, int lane) {
+  constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
+  constexpr int kGroupPitch = C::KV8 ? C::GP8 : C::GP;
+  const int g = lane;
+  const int j0 = g * C::R;
+  const int rows = (g < C::NG && j0 < nv) ? min(C::R, nv - j0) : 0;
+  mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * kRowBytes);
+  if (rows > 0) {
+    const long long pos0 = pbase + j0;
+    const size_t slot0 = static_cast<size_t>(pos0 % a.capacity);
+    const uint32_t goff = static_cast<uint32_t>(g) * kGroupPitch;
+    if (rows == C::R && slot0 + C::R <= static_cast<size_t>(a.capacity)) {
+      bulk_g2s(stage_dst + goff, src + slot0 * kRowBytes, C::R * kRowBytes, fb);
+    } else {  // a partial group, or one that wraps around the ring: row by row
+      for (int r = 0; r < rows; ++r) {
+        const size_t slot = static_cast<size_t>((pos0 + r) % a.capacity);
+        bulk_g2s(stage_dst + goff + r * kRowBytes, src + slot * kRowBytes, kRowBytes, fb);
+      }
+    }
+  }
+}
+
 template <class C, bool PERSIST = false>
 __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -360,6 +402,24 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int len_first = len_early ? a.lens[blockIdx.z] : 0;
   lpt_table(a, tid, C::THREADS, s_seq);
   __syncthreads();
+
+  // A sliding-window ring (window == capacity) is full in its steady state
+  // (len >= capacity): its band is then every slot, and this split's first
+  // tile is known before the length is. A per-split block issues that tile's
+  // copies at once, into stage 0; if the ring turns out not to be full, the
+  // stage is waited for and dropped, and the real tiles start at stage 1.
+  const bool spec = len_early && a.cluster == 1 && a.window > 0 && a.window >= a.capacity;
+  int spec_nv = 0;
+  if (spec) {
+    const long long cf = chunk_of(a.capacity, a.num_splits, a.granule);
+    const long long sp0 = static_cast<long long>(blockIdx.x) * cf;
+    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), min(cf, a.capacity - sp0))));
+    if (spec_nv > 0 && warp >= C::NWC) {
+      const bool is_k = warp == C::NWC;
+      produce_tile<C>(a, producer_src<C>(a, is_k, blockIdx.z, blockIdx.y), smem_u32(smem + producer_ring<C>(is_k)),
+                      full0, sp0, spec_nv, lane);
+    }
+  }
 
   // One work item (sequence, KV head, split) per block, or with a persistent
   // grid a stream of them: the K producer's lane 0 takes the next item index
@@ -410,13 +470,20 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int band = band_of(len_early ? len_first : a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0,
                            &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
-  const long long p0 = lo + static_cast<long long>(s) * chunk;
-  const long long p1 = min(static_cast<long long>(lo) + band, p0 + chunk);
+  // With no window, or a window as long as the cache, the band's slots are
+  // always [0, band): the splits walk slots (start 0) instead of positions
+  // (start lo); the softmax does not depend on the order.
+  const long long start = (a.window <= 0 || a.window >= a.capacity) ? 0 : lo;
+  const long long p0 = start + static_cast<long long>(s) * chunk;
+  const long long p1 = min(start + band, p0 + chunk);
   const int CS = a.cluster;                 // blocks per cluster along the splits
   const bool direct = a.num_splits == CS;   // one block / cluster spans every split
   const int n = p0 < p1 ? static_cast<int>(p1 - p0) : 0;
+  const bool spec_hit = spec_nv > 0 && band == a.capacity;  // the speculative tile is this split's first
+  const bool spec_miss = spec_nv > 0 && !spec_hit;          // stage 0 holds copies to drop
 
   if (n == 0 && CS == 1) {
+    if (spec_miss) mbar_wait(full0, 0, failed);  // no copy may land after the block has left
     // len == 0: the output row is zero. With one block per band, or with the
     // fused merge (no block of an empty band ever merges), block 0 writes it.
     if (direct || (a.fused && band == 0 && s == 0)) {
@@ -433,8 +500,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   // In a cluster every block, even one with an empty slice (m = -inf, l = 0,
   // O = 0), takes part in the reduction at the end.
   const int ntiles = (n + C::T - 1) / C::T;
-  const int gbase = gnext;  // pipeline tiles of this block's earlier items
-  gnext += ntiles;
+  const int gbase = gnext + (spec_miss ? 1 : 0);  // pipeline tiles of this block's earlier items
+  gnext = gbase + ntiles;
 
   const int grp = lane >> 2, t4 = lane & 3;
   const int dbase = warp * C::DW;
@@ -453,42 +520,19 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     // Warp NWC streams K, warp NWC + 1 streams V: two issuing warps raise a
     // block's copy rate (a block's rate is set by the copies it issues).
     const bool is_k = warp == C::NWC;
-    const size_t head_row0 = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity;
-    // byte source of this warp's tensor, and the byte geometry of its ring
-    const unsigned char* src =
-        C::KV8 ? (is_k ? a.k8 : a.v8) + head_row0 * C::HS
-               : reinterpret_cast<const unsigned char*>((is_k ? a.k : a.v) + head_row0 * C::HS);
-    constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
-    constexpr int kGroupPitch = C::KV8 ? C::GP8 : C::GP;
+    const unsigned char* src = producer_src<C>(a, is_k, b, kvh);
     constexpr size_t kStageBytes = C::KV8 ? C::STAGE8_BYTES : C::STAGE_BYTES;
-    const size_t ring = C::KV8 ? (is_k ? C::OFF_K8 : C::OFF_V8) : (is_k ? C::OFF_K : C::OFF_V);
+    const size_t ring = producer_ring<C>(is_k);
     for (int i = 0; i < ntiles; ++i) {
+      if (spec_hit && i == 0) continue;  // already in flight in stage 0
       const int gi = gbase + i;
       const int st = gi % C::NSTAGE;
       if (gi >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((gi / C::NSTAGE) - 1) & 1, failed);
       if (persist && failed) continue;  // nothing waits for these copies any more
       const int nv = min(C::T, n - i * C::T);
       const long long pbase = p0 + static_cast<long long>(i) * C::T;
-      const uint32_t dst = smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes);
-      const uint32_t fb = full0 + 8 * st;
-      // lane g copies group g: rows [g*R, g*R + rows) of the tile
-      const int g = lane;
-      const int j0 = g * C::R;
-      const int rows = (g < C::NG && j0 < nv) ? min(C::R, nv - j0) : 0;
-      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(rows) * kRowBytes);
-      if (rows > 0) {
-        const long long pos0 = pbase + j0;
-        const size_t slot0 = static_cast<size_t>(pos0 % a.capacity);
-        const uint32_t goff = static_cast<uint32_t>(g) * kGroupPitch;
-        if (rows == C::R && slot0 + C::R <= static_cast<size_t>(a.capacity)) {
-          bulk_g2s(dst + goff, src + slot0 * kRowBytes, C::R * kRowBytes, fb);
-        } else {  // a partial group, or one that wraps around the ring: row by row
-          for (int r = 0; r < rows; ++r) {
-            const size_t slot = static_cast<size_t>((pos0 + r) % a.capacity);
-            bulk_g2s(dst + goff + r * kRowBytes, src + slot * kRowBytes, kRowBytes, fb);
-          }
-        }
-      }
+      produce_tile<C>(a, src, smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes), full0 + 8 * st, pbase,
+                      nv, lane);
     }
   } else {
   // -------------------------------------------------------------- consumers
@@ -554,6 +598,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 
   // ldmatrix lane addressing
   const int lrow = lane & 7, lmat = lane >> 3;
+  if (spec_miss) {  // drop the speculative stage: wait for its copies, then free it
+    mbar_wait(full0, 0, failed);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0);
+  }
 
   for (int i = 0; i < ntiles; ++i) {
     const int gi = gbase + i;
