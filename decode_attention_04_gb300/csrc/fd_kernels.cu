@@ -1316,8 +1316,10 @@ cudaError_t occupancy_tc(int* ctas) {
 }
 
 // Tile configurations (measured on GB300, per head dim): 8 groups of 2 KB per
-// tensor per stage (about 33 KB of K+V), three stages, two blocks per SM;
-// G <= 8 or G <= 16 query rows per group. Head dims 256 and 512 use eight
+// tensor per stage (about 33 KB of K+V), three stages; G <= 8 or G <= 16
+// query rows per group. The d128 and d256 tiles for G <= 8 and the d512 tiles
+// fit two blocks per SM (100-111 KB each); the d64 tiles and the 16-row d128
+// and d256 tiles (118-139 KB) fit one. Head dims 256 and 512 use eight
 // consumer warps (shorter per-warp dependency chains; the one-block-per-SM
 // MQA grids gained most). The head-dim-512, 16-row tile planned with one block
 // per SM uses 4 KB groups: 66 KB stages, ~218 KB of shared memory.

@@ -163,3 +163,15 @@ def test_fp8_extreme_magnitudes(q_mul, k_mul, v_mul):
     assert np.isfinite(got).all()
     tol = 2e-3 * max(1.0, v_mul)
     assert np.abs(got - ref).max() <= tol, np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("length", [0, 40, 1024, 3000])
+def test_fp8_ring_first_tile_copied_before_the_length(length):
+    """The E4M3 ring (window == capacity): a full ring uses the first tile
+    copied before the length arrived; a ring that is not full drops it."""
+    w = W("fp8_ring_spec", 1, 16, 8, 256, 1024, 1024, lens=(length,), seed=48)
+    q, k8, v8, ks, vs, lens = make_inputs_fp8(w)
+    for splits in (0, 5):
+        res = run_fp8(w, q, k8, v8, ks, vs, lens, splits=splits)
+        assert res["deverr"] == 0
+        check(res, oracle_ref_fp8(w, q, k8, v8, ks, vs, lens), what=f"len={length} S={splits}")

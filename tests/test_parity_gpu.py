@@ -336,3 +336,18 @@ def test_staged_merge_nan_in_scores_reaches_only_its_group():
     out = res["out32"]
     assert torch.isnan(out[1, G:]).all()
     assert torch.isfinite(out[1, :G]).all() and torch.isfinite(out[[0, 2, 3]]).all()
+
+
+@pytest.mark.parametrize("lens", [(0,), (1,), (100,), (1023,), (1024,), (5000,)])
+@pytest.mark.parametrize("splits", [0, 1, 7, 32])
+def test_ring_first_tile_copied_before_the_length(lens, splits):
+    """A ring (window == capacity) with one sequence: each split block copies
+    its first tile for a full ring before it knows the length. A ring that is
+    not full (len < capacity) drops those copies: empty slices (which wait for
+    them before leaving), partial slices, one split (the output written
+    directly) and len == 0 all match the oracle; full rings use the copies."""
+    w = W("ring_spec", 1, 16, 8, 256, 1024, 1024, lens=lens, seed=93)
+    q, k, v, lens_t = make_inputs(w)
+    res = run(w, q, k, v, lens_t, splits=splits)
+    assert res["deverr"] == 0
+    check(res, oracle_ref(w, q, k, v, lens_t), what=f"len={lens[0]} S={splits}")
