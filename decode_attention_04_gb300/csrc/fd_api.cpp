@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -267,6 +268,41 @@ int device_sms(int device, int* sms) {
   return FD_OK;
 }
 
+// Resident split blocks per SM and the largest schedulable cluster of the
+// tensor-core kernel for (device, HS, G, cache type): occupancy queries,
+// made once and cached (they sit on every fd_decode_attn call's host path).
+struct Occupancy {
+  int ctas = 0;
+  int max_cluster = 1;
+};
+std::map<std::tuple<int, int, int, bool>, Occupancy> g_occ;
+
+int device_occupancy(int device, int HS, int G, bool kv8, int* ctas, int* max_cluster) {
+  const auto key = std::make_tuple(device, HS, G, kv8);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) {
+      *ctas = it->second.ctas;
+      *max_cluster = it->second.max_cluster;
+      return FD_OK;
+    }
+  }
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return FD_ERR_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return FD_ERR_CUDA;
+  Occupancy o;
+  cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, G, kv8, &o.ctas);
+  if (e == cudaSuccess) e = fd::query_max_cluster(HS, G, kv8, &o.max_cluster);
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess || o.ctas <= 0) return FD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occ[key] = o;
+  *ctas = o.ctas;
+  *max_cluster = o.max_cluster;
+  return FD_OK;
+}
+
 // Library-owned workspaces, one per (device, stream), grow-only.
 struct Workspace {
   void* ptr = nullptr;
@@ -388,15 +424,9 @@ int fd_plan_kv(int B, int NH, int NKV, int HS, int capacity, int window, int max
   int sms = 0;
   rc = device_sms(device, &sms);
   if (rc != FD_OK) return rc;
-  int prev = -1;
-  if (cudaGetDevice(&prev) != cudaSuccess) return FD_ERR_CUDA;
-  if (prev != device && cudaSetDevice(device) != cudaSuccess) return FD_ERR_CUDA;
   int ctas = 0, max_cluster = 1;
-  const bool kv8 = kv_dtype == FD_KV_E4M3;
-  cudaError_t e = fd::query_ctas_per_sm(FD_PATH_TC, HS, NH / NKV, kv8, &ctas);
-  if (e == cudaSuccess) e = fd::query_max_cluster(HS, NH / NKV, kv8, &max_cluster);
-  if (prev != device) cudaSetDevice(prev);
-  if (e != cudaSuccess || ctas <= 0) return FD_ERR_CUDA;
+  rc = device_occupancy(device, HS, NH / NKV, kv_dtype == FD_KV_E4M3, &ctas, &max_cluster);
+  if (rc != FD_OK) return rc;
   return make_plan(B, NH, NKV, HS, capacity, window, max_len, sms, ctas, max_cluster, FD_PATH_AUTO, kv_dtype,
                    plan);
 }

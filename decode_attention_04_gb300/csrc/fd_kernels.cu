@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <utility>
 
@@ -1287,19 +1288,45 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Kernel attributes are set once per (kernel, device): the values never
+// change, and the driver call would otherwise sit on every launch's host path.
+template <auto Kernel>
+cudaError_t smem_attr_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};  // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <auto Kernel>
+cudaError_t cluster_attr_once() {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 template <class C>
 cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
   static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM));
+  cudaError_t e = smem_attr_once<split_tc_kernel<C>>(static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   if (a.cluster > 8) {
-    e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cluster_attr_once<split_tc_kernel<C>>();
     if (e != cudaSuccess) return e;
   }
   if (a.persistent > 0) {
-    e = cudaFuncSetAttribute(split_tc_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::SMEM));
+    e = smem_attr_once<split_tc_kernel<C, true>>(static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     return launch_pdl(split_tc_kernel<C, true>, dim3(a.persistent), dim3(C::THREADS), C::SMEM, stream, 1, a);
   }
@@ -1309,8 +1336,7 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
 
 template <class C>
 cudaError_t occupancy_tc(int* ctas) {
-  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM));
+  cudaError_t e = smem_attr_once<split_tc_kernel<C>>(static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
 }
@@ -1474,8 +1500,7 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
     return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
   }
   const size_t msmem = merge_smem_bytes(a.num_splits / a.cluster);
-  e = cudaFuncSetAttribute(merge_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(msmem));
+  e = smem_attr_once<merge_staged_kernel>(static_cast<int>(merge_smem_bytes(kMergeStageMax)));
   if (e != cudaSuccess) return e;
   dim3 mgrid(a.HS / kMergeDims, a.NH, a.B);
   return launch_pdl(merge_staged_kernel, mgrid, dim3(kMergeThreads), msmem, stream, 1, a);
