@@ -119,7 +119,12 @@ int group_rule(const fd_plan_t& p) {
   const long long G = p.NH / p.NKV;
   const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
   if (p.path == FD_PATH_UMMA) return 16384;  // one TMA box: 128 positions x 64 dims
-  if (p.kv_dtype == FD_KV_E4M3) return p.HS == 256 ? 1024 : 2048;
+  if (p.kv_dtype == FD_KV_E4M3) {
+    // 1 KB groups for head dim 256, and for 64 / 128 when the plan cut the
+    // band into whole short tiles
+    const int short_tile = fd::tc_short_tile_positions(p.HS);
+    return (p.HS == 256 || (short_tile > 0 && p.granule == short_tile)) ? 1024 : 2048;
+  }
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
 }
 
@@ -198,7 +203,11 @@ int make_plan(int B, int NH, int NKV, int HS, int capacity, int window, int max_
   // under two tiles; longer pieces keep single positions as the granule, so
   // rounding never leaves SMs idle.
   const int tile = fd::plan_granule(path, HS, kv_dtype == FD_KV_E4M3);
-  const int granule = (max_band + s_fill - 1) / s_fill < 2 * tile ? tile : 1;
+  int granule = (max_band + s_fill - 1) / s_fill < 2 * tile ? tile : 1;
+  // An E4M3 cache with head dim 64 or 128 has a half-length tile (1 KB copy
+  // groups) for such short bands: twice the blocks for the same band.
+  const int short_tile = fd::tc_short_tile_positions(HS);
+  if (kv_dtype == FD_KV_E4M3 && path == FD_PATH_TC && granule == tile && short_tile > 0) granule = short_tile;
   auto chunk_for = [&](long long S) {
     long long c = (max_band + S - 1) / S;
     c = (c + granule - 1) / granule * granule;

@@ -42,6 +42,9 @@ struct LaunchArgs {
 // Positions per pipeline tile of the tensor-core kernel for head size HS, and
 // the chunk granule the plan uses for it.
 int tc_tile_positions(int HS, bool kv8);
+// Positions of the short-band E4M3 tile (1 KB groups) for head sizes 64 and
+// 128; 0 for the others.
+int tc_short_tile_positions(int HS);
 int plan_granule(int path, int HS, bool kv8);
 
 // Resident CTAs per SM of the kernel a plan would launch (occupancy query).

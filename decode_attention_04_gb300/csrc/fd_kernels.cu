@@ -1373,14 +1373,25 @@ using Tc256x2f = TcCfg<256, 2, 8, 4, 2048, true>;
 using Tc512x1f = TcCfg<512, 1, 4, 2, 4096, true>;
 using Tc512x2f = TcCfg<512, 2, 4, 2, 4096, true>;
 using Tc512x2f8 = TcCfg<512, 2, 8, 2, 4096, true>;  // one block per SM
+// Head dims 64 and 128 with short bands (the plan's whole-tile splits): 1 KB
+// E4M3 groups in four stages, half the default tile, so a short band spreads
+// over twice as many blocks.
+using Tc64x1fs = TcCfg<64, 1, 2, 4, 2048, true>;
+using Tc64x2fs = TcCfg<64, 2, 2, 4, 2048, true>;
+using Tc128x1fs = TcCfg<128, 1, 4, 4, 2048, true>;
+using Tc128x2fs = TcCfg<128, 2, 4, 4, 2048, true>;
 
 template <template <class> class Fn, class... Args>
 cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, int warps, Args&&... args) {
   const bool two = G > 8;
   if (kv8) {
     switch (HS) {
-      case 64: return two ? Fn<Tc64x2f>::run(args...) : Fn<Tc64x1f>::run(args...);
-      case 128: return two ? Fn<Tc128x2f>::run(args...) : Fn<Tc128x1f>::run(args...);
+      case 64:
+        if (group_bytes == 1024) return two ? Fn<Tc64x2fs>::run(args...) : Fn<Tc64x1fs>::run(args...);
+        return two ? Fn<Tc64x2f>::run(args...) : Fn<Tc64x1f>::run(args...);
+      case 128:
+        if (group_bytes == 1024) return two ? Fn<Tc128x2fs>::run(args...) : Fn<Tc128x1fs>::run(args...);
+        return two ? Fn<Tc128x2f>::run(args...) : Fn<Tc128x1f>::run(args...);
       case 256: return two ? Fn<Tc256x2f>::run(args...) : Fn<Tc256x1f>::run(args...);
       case 512:
         if (!two) return Fn<Tc512x1f>::run(args...);
@@ -1445,6 +1456,14 @@ struct OccFn {
 };
 
 }  // namespace
+
+int tc_short_tile_positions(int HS) {
+  switch (HS) {
+    case 64: return Tc64x1fs::T;
+    case 128: return Tc128x1fs::T;
+    default: return 0;
+  }
+}
 
 int tc_tile_positions(int HS, bool kv8) {
   switch (HS) {

@@ -109,7 +109,8 @@ enum {
  * into pieces under two tiles of the tensor-core kernel, chunks are whole
  * tiles (`granule` = the tile's positions: a split shorter than a tile costs
  * a full tile's latency and adds a partial), so a short band gets fewer
- * splits; otherwise the granule is 1. On
+ * splits; otherwise the granule is 1. An E4M3 cache with head dim 64 or 128
+ * then uses a half-length tile (1 KB copy groups: 128 or 64 positions). On
  * the device each sequence cuts its own band into chunks of
  * ceil(band_b / num_splits) positions rounded up to the granule, so a short
  * sequence uses fewer, not emptier, splits.

@@ -198,7 +198,12 @@ def test_e4m3_plan_matches_bf16_rule_with_half_the_bytes(name, lib):
     w = WORKLOADS[name]
     p8, p16 = _plan_kv(w), _plan(w)
     assert p8.kv_dtype == fd.FD_KV_E4M3 and p16.kv_dtype == fd.FD_KV_BF16
-    assert p8.group_bytes == (1024 if w.HS == 256 else 2048) and p8.path == fd.FD_PATH_TC
+    # 1 KB E4M3 groups for head dim 256, and for 64 / 128 when the band is cut
+    # into whole short tiles (the half-length tile: 64 positions at d128)
+    short = w.HS in (64, 128) and p8.granule > 1
+    assert p8.group_bytes == (1024 if w.HS == 256 or short else 2048) and p8.path == fd.FD_PATH_TC
+    if short:
+        assert p8.granule == {64: 128, 128: 64}[w.HS]
     # consumer warps: 8 for the E4M3 head-dim-512 MQA tile only when the grid
     # is one block per SM; bf16 head dims 256/512 (16-row tiles) use 8
     blocks = w.B * w.NKV * p8.num_splits
@@ -359,3 +364,19 @@ def test_persistent_plan_checked_before_any_cuda_call(lib):
     rc = lib.fd_decode_attn_ex(ctypes.byref(q), dummy, q.workspace_bytes, None, dummy, dummy, dummy, dummy,
                                dummy, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
     assert rc == fd.FD_ERR_INVALID_ARG
+
+
+def test_e4m3_short_band_tile(lib):
+    """An E4M3 cache with head dim 128 and a short band takes the half-length
+    tile (1 KB groups, 64 positions): twice the splits of the 2 KB tile; long
+    bands keep 2 KB groups; a forced kernel family returns to the default."""
+    t = WORKLOADS["llama_tiny"]
+    p = _plan_kv(t)
+    assert (p.granule, p.group_bytes) == (64, 1024)
+    assert p.num_splits == -(-t.capacity // 64)
+    r = _plan_kv(WORKLOADS["llama_ragged"])
+    assert (r.granule, r.group_bytes) == (1, 2048)
+    fd.fd_plan_override(p, 0, fd.FD_PATH_TC)  # same family: unchanged
+    assert p.group_bytes == 1024
+    q = _plan_kv(WORKLOADS["gemma_local_ring"])
+    assert q.group_bytes == 1024 and q.granule == 32  # head dim 256 keeps its own 1 KB tile
