@@ -138,6 +138,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Hint: bring [p, p + bytes) into L2 (no data reaches the thread; p and
+// bytes multiples of 16). A later load still reads whatever L2 then holds, so
+// the hint may precede a wait for the kernel that writes those bytes.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with
 // cudaLaunchAttributeProgrammaticStreamSerialization may start while the
 // previous kernel on the stream is still running. It must wait for that

@@ -395,26 +395,38 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     sM[i] = kNegInf;
     sL[i] = 0.f;
   }
+  // A sliding-window ring (window == capacity) is full in its steady state
+  // (len >= capacity): its band is then every slot, and this split's first
+  // tile is known before the length is. A per-split block whose sequence
+  // needs no ordering table asks L2 for that tile while the previous kernel
+  // is still running (a hint only: the copies that use the tile come after
+  // the dependency wait), then, past the wait, issues the tile's copies at
+  // once, into stage 0; if the ring turns out not to be full, the stage is
+  // waited for and dropped, and the real tiles start at stage 1.
+  const bool len_early = !PERSIST && !lpt_ordered(a);
+  const bool spec = len_early && a.cluster == 1 && a.window > 0 && a.window >= a.capacity;
+  int spec_nv = 0;
+  long long sp0 = 0;
+  if (spec) {
+    const long long cf = chunk_of(a.capacity, a.num_splits, a.granule);
+    sp0 = static_cast<long long>(blockIdx.x) * cf;
+    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), min(cf, a.capacity - sp0))));
+    if (spec_nv > 0 && warp >= C::NWC && lane == 0) {
+      constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
+      const bool is_k = warp == C::NWC;
+      prefetch_l2(producer_src<C>(a, is_k, blockIdx.z, blockIdx.y) + sp0 * kRowBytes,
+                  static_cast<uint32_t>(spec_nv) * kRowBytes);
+    }
+  }
   grid_dependency_wait();
   grid_launch_dependents();
-  // A per-split block whose sequence needs no ordering table reads its length
-  // before the barrier, so the load's latency overlaps the barrier wait.
-  const bool len_early = !PERSIST && !lpt_ordered(a);
+  // Such a block also reads its length before the barrier, so the load's
+  // latency overlaps the barrier wait.
   const int len_first = len_early ? a.lens[blockIdx.z] : 0;
   lpt_table(a, tid, C::THREADS, s_seq);
   __syncthreads();
 
-  // A sliding-window ring (window == capacity) is full in its steady state
-  // (len >= capacity): its band is then every slot, and this split's first
-  // tile is known before the length is. A per-split block issues that tile's
-  // copies at once, into stage 0; if the ring turns out not to be full, the
-  // stage is waited for and dropped, and the real tiles start at stage 1.
-  const bool spec = len_early && a.cluster == 1 && a.window > 0 && a.window >= a.capacity;
-  int spec_nv = 0;
   if (spec) {
-    const long long cf = chunk_of(a.capacity, a.num_splits, a.granule);
-    const long long sp0 = static_cast<long long>(blockIdx.x) * cf;
-    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), min(cf, a.capacity - sp0))));
     if (spec_nv > 0 && warp >= C::NWC) {
       const bool is_k = warp == C::NWC;
       produce_tile<C>(a, producer_src<C>(a, is_k, blockIdx.z, blockIdx.y), smem_u32(smem + producer_ring<C>(is_k)),
