@@ -418,6 +418,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
                   static_cast<uint32_t>(spec_nv) * kRowBytes);
     }
   }
+  // The block's query rows (G consecutive heads, contiguous) do not depend on
+  // the length: ask L2 for them too.
+  if (len_early && tid == 0)
+    prefetch_l2(a.q + (static_cast<size_t>(blockIdx.z) * a.NH + static_cast<size_t>(blockIdx.y) * G) * C::HS,
+                static_cast<uint32_t>(G) * C::HS * 2);
   grid_dependency_wait();
   grid_launch_dependents();
   // Such a block also reads its length before the barrier, so the load's
