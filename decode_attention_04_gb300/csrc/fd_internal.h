@@ -35,6 +35,8 @@ struct LaunchArgs {
   int num_splits;           // S
   int cluster;              // blocks per cluster along the splits (S % cluster == 0)
   int granule;              // chunk rounding, positions
+  int tile_stride;          // > 0: the split kernel dealt T = tile_stride position tiles to the splits in
+                            // turn (bands of slots [0, band)); 0: consecutive chunks (set at launch)
   int path;                 // FD_PATH_SIMT / FD_PATH_TC / FD_PATH_UMMA
   float scale_log2;         // scale * log2(e)
 };

@@ -395,22 +395,23 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     sM[i] = kNegInf;
     sL[i] = 0.f;
   }
-  // A sliding-window ring (window == capacity) is full in its steady state
-  // (len >= capacity): its band is then every slot, and this split's first
-  // tile is known before the length is. A per-split block whose sequence
-  // needs no ordering table asks L2 for that tile while the previous kernel
-  // is still running (a hint only: the copies that use the tile come after
-  // the dependency wait), then, past the wait, issues the tile's copies at
-  // once, into stage 0; if the ring turns out not to be full, the stage is
-  // waited for and dropped, and the real tiles start at stage 1.
+  // With no window, or a window as long as the cache, a band's slots are
+  // [0, band), and the splits take its T-position tiles in turn (split s:
+  // tiles s, s + S, s + 2S, ...), so a split's first tile, slots
+  // [s*T, s*T + T), is known before the length is. A per-split block whose
+  // sequence needs no ordering table asks L2 for that tile while the previous
+  // kernel is still running (a hint only: the copies that use the tile come
+  // after the dependency wait), then, past the wait, issues the tile's copies
+  // at once, into stage 0; if the band turns out not to hold the whole tile,
+  // the stage is waited for and dropped, and the real tiles start at stage 1.
+  const bool tiled = a.window <= 0 || a.window >= a.capacity;
   const bool len_early = !PERSIST && !lpt_ordered(a);
-  const bool spec = len_early && a.cluster == 1 && a.window > 0 && a.window >= a.capacity;
+  const bool spec = len_early && a.cluster == 1 && tiled;
   int spec_nv = 0;
   long long sp0 = 0;
   if (spec) {
-    const long long cf = chunk_of(a.capacity, a.num_splits, a.granule);
-    sp0 = static_cast<long long>(blockIdx.x) * cf;
-    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), min(cf, a.capacity - sp0))));
+    sp0 = static_cast<long long>(blockIdx.x) * C::T;
+    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), a.capacity - sp0)));
     if (spec_nv > 0 && warp >= C::NWC && lane == 0) {
       constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
       const bool is_k = warp == C::NWC;
@@ -487,20 +488,29 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   int lo;
   const int band = band_of(len_early ? len_first : a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0,
                            &lo);
-  const int chunk = chunk_of(band, a.num_splits, a.granule);
-  // With no window, or a window as long as the cache, the band's slots are
-  // always [0, band): the splits walk slots (start 0) instead of positions
-  // (start lo); the softmax does not depend on the order.
-  const long long start = (a.window <= 0 || a.window >= a.capacity) ? 0 : lo;
-  const long long p0 = start + static_cast<long long>(s) * chunk;
-  const long long p1 = min(start + band, p0 + chunk);
+  // This split's tiles: tile i holds positions [tile_pos(i), + tile_nv(i)).
+  // Tiled bands (slots [0, band)): tiles s, s + S, ... of the band; other
+  // bands: the consecutive positions [lo + s*chunk, ...) cut into tiles. The
+  // softmax does not depend on the order.
+  const int S = a.num_splits;
+  const int nt_band = (band + C::T - 1) / C::T;
+  const int chunk = chunk_of(band, S, a.granule);
+  const long long p0 = lo + static_cast<long long>(s) * chunk;
+  const int n = tiled ? 0 : static_cast<int>(max(0ll, min(static_cast<long long>(lo) + band, p0 + chunk) - p0));
+  const int ntiles = tiled ? (s < nt_band ? (nt_band - s + S - 1) / S : 0) : (n + C::T - 1) / C::T;
+  const int nact = tiled ? min(S, nt_band) : active_splits(band, chunk);  // splits with work
+  auto tile_pos = [&](int i) -> long long {
+    return tiled ? static_cast<long long>(s + i * S) * C::T : p0 + static_cast<long long>(i) * C::T;
+  };
+  auto tile_nv = [&](int i) -> int {
+    return tiled ? min(C::T, band - (s + i * S) * C::T) : min(C::T, n - i * C::T);
+  };
   const int CS = a.cluster;                 // blocks per cluster along the splits
-  const bool direct = a.num_splits == CS;   // one block / cluster spans every split
-  const int n = p0 < p1 ? static_cast<int>(p1 - p0) : 0;
-  const bool spec_hit = spec_nv > 0 && band == a.capacity;  // the speculative tile is this split's first
-  const bool spec_miss = spec_nv > 0 && !spec_hit;          // stage 0 holds copies to drop
+  const bool direct = S == CS;              // one block / cluster spans every split
+  const bool spec_hit = spec_nv > 0 && ntiles > 0 && tile_nv(0) == spec_nv;  // the speculative tile is tile 0
+  const bool spec_miss = spec_nv > 0 && !spec_hit;                           // stage 0 holds copies to drop
 
-  if (n == 0 && CS == 1) {
+  if (ntiles == 0 && CS == 1) {
     if (spec_miss) mbar_wait(full0, 0, failed);  // no copy may land after the block has left
     // len == 0: the output row is zero. With one block per band, or with the
     // fused merge (no block of an empty band ever merges), block 0 writes it.
@@ -517,7 +527,6 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   // In a cluster every block, even one with an empty slice (m = -inf, l = 0,
   // O = 0), takes part in the reduction at the end.
-  const int ntiles = (n + C::T - 1) / C::T;
   const int gbase = gnext + (spec_miss ? 1 : 0);  // pipeline tiles of this block's earlier items
   gnext = gbase + ntiles;
 
@@ -547,8 +556,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       const int st = gi % C::NSTAGE;
       if (gi >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((gi / C::NSTAGE) - 1) & 1, failed);
       if (persist && failed) continue;  // nothing waits for these copies any more
-      const int nv = min(C::T, n - i * C::T);
-      const long long pbase = p0 + static_cast<long long>(i) * C::T;
+      const int nv = tile_nv(i);
+      const long long pbase = tile_pos(i);
       produce_tile<C>(a, src, smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes), full0 + 8 * st, pbase,
                       nv, lane);
     }
@@ -626,7 +635,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     const int gi = gbase + i;
     const int st = gi % C::NSTAGE;
     mbar_wait(full0 + 8 * st, (gi / C::NSTAGE) & 1, failed);
-    const int nv = min(C::T, n - i * C::T);  // valid tile positions: [0, nv)
+    const int nv = tile_nv(i);  // valid tile positions: [0, nv)
     const unsigned char* tK = smem + C::OFF_K + static_cast<size_t>(st) * C::STAGE_BYTES;
     unsigned char* tV = smem + C::OFF_V + static_cast<size_t>(st) * C::STAGE_BYTES;
     // E4M3 stage (KV8)
@@ -881,7 +890,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     // wraps to zero as the last block takes it, so it is zero again for the
     // next call.
     __shared__ int s_last;
-    const int nsplit = active_splits(band, chunk);
+    const int nsplit = nact;
     named_bar_sync(1, C::CTHREADS);  // every thread's partial stores precede ...
     if (tid == 0) {
       __threadfence();  // ... this fence (cumulative), so they are visible before the count
@@ -1106,7 +1115,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   int lo;
   const int band = band_of(len_b, a.capacity, a.window, false, &lo);
   const int chunk = chunk_of(band, a.num_splits, a.granule);
-  const int ns = (active_splits(band, chunk) + CS - 1) / CS;
+  const int act = a.tile_stride > 0 ? min(a.num_splits, (band + a.tile_stride - 1) / a.tile_stride)
+                                    : active_splits(band, chunk);
+  const int ns = (act + CS - 1) / CS;
   float mw = kNegInf, lw = 0.f, acc = 0.f;
   for (int s0 = warp; s0 < ns; s0 += kMergeWarps * kMergeBatch) {
     if (s0 != warp) {
@@ -1471,6 +1482,13 @@ template <class C>
 struct OccFn {
   static cudaError_t run(int* ctas) { return occupancy_tc<C>(ctas); }
 };
+template <class C>
+struct TileFn {
+  static cudaError_t run(int* t) {
+    *t = C::T;
+    return cudaSuccess;
+  }
+};
 
 }  // namespace
 
@@ -1514,9 +1532,15 @@ cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster) {
   return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, 0, cluster);
 }
 
-cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream) {
-  const int G = a.NH / a.NKV;
+cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
+  const int G = args.NH / args.NKV;
   cudaError_t e;
+  LaunchArgs a = args;
+  a.tile_stride = 0;
+  if (a.path == FD_PATH_TC && (a.window <= 0 || a.window >= a.capacity)) {
+    e = with_tc_cfg<TileFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, &a.tile_stride);
+    if (e != cudaSuccess) return e;
+  }
   if (a.path == FD_PATH_SIMT) {
     const size_t sm = simt_smem_bytes(G, a.HS);
     e = cudaFuncSetAttribute(split_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
