@@ -110,7 +110,10 @@ enum {
  * tiles (`granule` = the tile's positions: a split shorter than a tile costs
  * a full tile's latency and adds a partial), so a short band gets fewer
  * splits; otherwise the granule is 1. An E4M3 cache with head dim 64 or 128
- * then uses a half-length tile (1 KB copy groups: 128 or 64 positions). On
+ * then uses a half-length tile (1 KB copy groups: 128 or 64 positions). With
+ * no window, or a window as long as the cache, a band occupies slots
+ * [0, band) and the tensor-core kernel deals its tiles to the splits in turn
+ * (split s: tiles s, s + S, ...) instead of cutting chunks. On
  * the device each sequence cuts its own band into chunks of
  * ceil(band_b / num_splits) positions rounded up to the granule, so a short
  * sequence uses fewer, not emptier, splits.
