@@ -202,11 +202,37 @@ def fd_workspace_bytes(plan: fd_plan_t) -> int:
     return load_library().fd_workspace_bytes(ctypes.byref(plan))
 
 
+_fast_mod = None
+_fast_for = None  # the ctypes handle the compiled entries belong to
+
+
+def _fast():
+    """The compiled CPython entries (``_fdfast``, linked to the in-tree
+    libfd.so) when they were built and that library is the one loaded; else
+    None, and calls go through ctypes."""
+    global _fast_mod, _fast_for
+    lib = load_library()
+    if _fast_for is not lib:
+        _fast_for, _fast_mod = lib, None
+        if Path(getattr(lib, "_name", "")).resolve() == LIB_PATH.resolve():
+            try:
+                from . import _fdfast
+                _fast_mod = _fdfast
+            except ImportError:
+                _fast_mod = None
+    return _fast_mod
+
+
 def fd_decode_attn(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale,
                    stream=None) -> None:
-    _check(load_library().fd_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lens),
-                                         B, NH, NKV, HS, capacity, window, float(scale), _stream(stream)),
-           "fd_decode_attn")
+    f = _fast()
+    if f is not None:
+        rc = f.decode_attn(_ptr(q) or 0, _ptr(k_cache) or 0, _ptr(v_cache) or 0, _ptr(out) or 0, _ptr(lens) or 0,
+                           B, NH, NKV, HS, capacity, window, float(scale), _stream(stream) or 0)
+    else:
+        rc = load_library().fd_decode_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lens),
+                                           B, NH, NKV, HS, capacity, window, float(scale), _stream(stream))
+    _check(rc, "fd_decode_attn")
 
 
 def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens,
@@ -220,10 +246,16 @@ def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k
 
 def fd_decode_attn_fp8(q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, capacity, window, scale,
                        stream=None) -> None:
-    _check(load_library().fd_decode_attn_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(out),
-                                             _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
-                                             _stream(stream)),
-           "fd_decode_attn_fp8")
+    f = _fast()
+    if f is not None:
+        rc = f.decode_attn_fp8(_ptr(q) or 0, _ptr(k8) or 0, _ptr(v8) or 0, _ptr(k_scale) or 0, _ptr(v_scale) or 0,
+                               _ptr(out) or 0, _ptr(lens) or 0, B, NH, NKV, HS, capacity, window, float(scale),
+                               _stream(stream) or 0)
+    else:
+        rc = load_library().fd_decode_attn_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(out),
+                                               _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
+                                               _stream(stream))
+    _check(rc, "fd_decode_attn_fp8")
 
 
 def fd_decode_attn_fp8_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k8, v8, k_scale, v_scale, out,

@@ -380,3 +380,19 @@ def test_e4m3_short_band_tile(lib):
     assert p.group_bytes == 1024
     q = _plan_kv(WORKLOADS["gemma_local_ring"])
     assert q.group_bytes == 1024 and q.granule == 32  # head dim 256 keeps its own 1 KB tile
+
+
+def test_compiled_entries_return_the_library_status(lib):
+    """The compiled CPython entries (built where Python headers exist) call
+    the same loaded libfd.so as ctypes: argument errors come back as the same
+    status codes, before any CUDA call."""
+    f = fd._fast()
+    if f is None:
+        pytest.skip("compiled entries not built here")
+    cases = [(0, 0, 0, 0, 0, 1, 16, 8, 256, 64, 0, 0.0, 0),          # null pointers
+             (16, 16, 16, 16, 16, 1, 16, 8, 96, 64, 0, 0.0, 0),      # unsupported head size
+             (16, 16, 16, 16, 16, 1, 16, 8, 256, 64, 65, 0.0, 0)]    # window > capacity
+    for c in cases:
+        assert f.decode_attn(*c) == lib.fd_decode_attn(*c) != fd.FD_OK
+    c8 = (0, 0, 0, 0, 0, 0, 0, 1, 16, 8, 256, 64, 0, 0.0, 0)
+    assert f.decode_attn_fp8(*c8) == lib.fd_decode_attn_fp8(*c8) == fd.FD_ERR_INVALID_ARG
