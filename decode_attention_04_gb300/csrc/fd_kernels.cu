@@ -2,12 +2,12 @@
 //
 // The method is the Flash-Decoding formulation of "Hand-Writing Gemma 4
 // Flash-Decoding + an FP4 Matvec Bonus (Part 2)", section "One KV head breaks
-// the textbook": every (sequence b, KV head, split s) thread block walks the
-// absolute positions of its slice of the live band [max(0, len - W), len),
-// reads position p from cache slot p % capacity, and leaves an unnormalised
-// (O, m, l) partial; a merge kernel combines the partials with the
-// online-softmax rule. Softmax state is rescaled once per tile of positions,
-// not once per position (same section, last bullet).
+// the textbook": every (sequence b, KV head, split s) thread block takes its
+// share of the live band [max(0, len - W), len), reads position p from cache
+// slot p % capacity, and leaves an unnormalised (O, m, l) partial; a merge
+// kernel combines the partials with the online-softmax rule. Softmax state is
+// rescaled once per tile of positions, not once per position (same section,
+// last bullet).
 //
 // Kernels:
 //   split_simt_kernel  per-position fp32 kernel; the plain reference GPU path.
@@ -19,7 +19,9 @@
 //                      positions fill the 16-row side and the G <= 16 query
 //                      rows the 8-wide side), rescale once per tile, and
 //                      accumulate O^T = V^T P^T on the tensor cores.
-//   merge_kernel       online-softmax merge of the S partials of each row.
+//   merge_kernel       online-softmax merge of the S partials of each row
+//                      (few rows); merge_staged_kernel, the same for many rows,
+//                      with the partials brought into shared memory.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -203,8 +205,8 @@ size_t simt_smem_bytes(int G, int HS) {
 // groups of R consecutive positions, GROUP_BYTES (2 or 4 KB) per group, so one
 // bulk copy moves a whole group: a block's copy rate is set by the number of
 // copies it issues (on GB300, about 15 / 23 / 33 / 45 GB/s per block with
-// 0.5 / 1 / 2 / 4 KB copies), not by their bytes. Groups are 16 bytes apart beyond their R rows. Row i of
-// group g holds tile position g*R + i.
+// 0.5 / 1 / 2 / 4 KB copies), not by their bytes. Groups are 16 bytes apart
+// beyond their R rows. Row i of group g holds tile position g*R + i.
 //
 // The MMAs walk the tile in a permuted order: MMA row m takes group m % NG,
 // row m / NG. Eight consecutive MMA rows then sit in eight different groups,
