@@ -120,7 +120,9 @@ enum {
  *
  * With G >= 8 query rows per KV head a partial (G x HS floats) is costly
  * next to a split's K/V bytes, and the plan fills each SM once instead of
- * with every resident block.
+ * with every resident block, unless that would put more than ~2 MiB of K+V
+ * in a split: then it fills every resident block slot once, with up to
+ * ~4 MiB per split, before adding waves.
  *
  * Fused merge (opt-in through fd_plan_override; plans use fused = 0): when a
  * group has few partials (G * S <= 480), the last split block of each
