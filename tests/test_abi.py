@@ -396,3 +396,16 @@ def test_compiled_entries_return_the_library_status(lib):
         assert f.decode_attn(*c) == lib.fd_decode_attn(*c) != fd.FD_OK
     c8 = (0, 0, 0, 0, 0, 0, 0, 1, 16, 8, 256, 64, 0, 0.0, 0)
     assert f.decode_attn_fp8(*c8) == lib.fd_decode_attn_fp8(*c8) == fd.FD_ERR_INVALID_ARG
+
+
+def test_plan_long_bands_with_large_groups_fill_every_slot_once(lib):
+    """G >= 8: one block per SM while a split stays under ~2 MiB of K+V; a
+    longer band (MQA, 4 x 131072 positions) first takes every resident slot
+    once with up to ~4 MiB per split; B = 1 MQA at 32K keeps one per SM."""
+    w = WORKLOADS["gemma_mqa_long"]
+    p = _plan(w)
+    assert w.G >= 8 and p.num_splits * w.B * w.NKV == 152 * 2
+    assert -(-w.capacity // p.num_splits) * w.HS * 4 <= 4 << 20
+    assert _plan(WORKLOADS["gemma_global_mqa_32k"]).num_splits == 152
+    one_per_sm = _plan(w, ctas=1)  # no second slot per SM: waves at the 2 MiB bound
+    assert -(-w.capacity // one_per_sm.num_splits) * w.HS * 4 <= (2 << 20) + w.HS * 4
