@@ -587,6 +587,13 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     }
 
   float sl2 = a.scale_log2;  // score scale, log2 units
+  // E4M3: this head's K and V scales, loaded now so their latency is not on
+  // the path to the first scores or to the epilogue
+  [[maybe_unused]] float k_scale = 1.f, v_scale = 1.f;
+  if constexpr (C::KV8) {
+    k_scale = a.k_scale[static_cast<size_t>(b) * a.NKV + kvh];
+    v_scale = a.v_scale[static_cast<size_t>(b) * a.NKV + kvh];
+  }
   if constexpr (C::KV8) {
     // fp16 MMAs: Q goes to fp16 with one power-of-two scale per block, so the
     // block's largest |q| lands in [2^13, 2^14) and no product can overflow;
@@ -620,7 +627,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
           qf[ks][nt][e] = pack_f16x2(ldexpf(bf16_bits_to_f32(static_cast<uint16_t>(x & 0xffffu)), eq),
                                      ldexpf(bf16_bits_to_f32(static_cast<uint16_t>(x >> 16)), eq));
         }
-    sl2 = a.scale_log2 * a.k_scale[static_cast<size_t>(b) * a.NKV + kvh] * ldexpf(1.f, -eq);
+    sl2 = a.scale_log2 * k_scale * ldexpf(1.f, -eq);
   }
 
   float m_run = kNegInf, l_run = 0.f;
@@ -843,7 +850,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
 
     if constexpr (C::KV8) {  // O in dequantised units: times this head's V scale
-      const float vs = a.v_scale[static_cast<size_t>(b) * a.NKV + kvh];
+      const float vs = v_scale;
 #pragma unroll
       for (int mt = 0; mt < C::KD; ++mt)
 #pragma unroll
