@@ -154,7 +154,7 @@ enum {
  */
 typedef struct {
   int num_splits;          /* S: grid splits per (sequence, KV head) */
-  int path;                /* FD_PATH_SIMT or FD_PATH_TC */
+  int path;                /* FD_PATH_SIMT, FD_PATH_TC or FD_PATH_UMMA */
   int cluster;             /* blocks per cluster along the splits; divides S; 1 = none */
   int granule;             /* chunk rounding on the device, positions: 1, or the tile for short bands */
   int max_band;            /* band bound the plan was sized for */
