@@ -6,6 +6,23 @@ Every function here has the name of the C entry point it wraps
 device pointers, the current torch stream becomes the CUDA stream, non-zero
 status codes become FdError. All arithmetic runs in libfd.so's kernels. There
 is no fallback: if libfd.so is missing or a call fails, an exception is raised.
+Where Python headers were available at build time, fd_decode_attn and
+fd_decode_attn_fp8 go through the small compiled module _fdfast (the same
+libfd.so, less host time per call); elsewhere they go through ctypes.
+
+Typical use in a decode loop (every layer its own cache; lens counts the
+current token, whose K/V are already in the cache):
+
+    import torch, decode_attention_04_gb300 as fd
+    # q: bf16 [B, NH, HS]; k, v: bf16 [B, NKV, capacity, HS]; lens: int32 [B]
+    out = fd.decode_attention(q, k, v, lens, window=1024)      # allocates out
+    fd.fd_decode_attn(q, k, v, out, lens, B, NH, NKV, HS, capacity, window,
+                      0.0)                                      # into out
+
+The first call for a (device, stream) sizes the library's workspace; later
+calls may be captured in a CUDA graph. fd_plan / fd_decode_attn_ex take an
+explicit plan and workspace instead (nothing allocated by the library), and
+fd_decode_attn_noalloc uses a fixed scratch array compiled into libfd.so.
 """
 
 from __future__ import annotations
