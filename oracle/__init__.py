@@ -10,8 +10,11 @@ Matvec Bonus (Part 2)", sections "One KV head breaks the textbook" and "The test
 that catches what parity misses"). This module only compiles it with g++ and
 marshals numpy arrays into it.
 
-Pinning: every function here is pinned by ``tests/test_oracle_pins.py``
-(brute force, a library routine, closed forms and invariants). No function is
+Pinning: the attention entry points are pinned by ``tests/test_oracle_pins.py``
+(brute force, a library routine, closed forms and invariants); the bf16
+helpers ``bf16_round`` and ``bf16_bits_to_f64`` by ``tests/test_oracle_bf16.py``
+(torch's conversions where they round once, an exact rational
+round-to-nearest-even, every bit pattern, planted mistakes). No function is
 "parity unpinned".
 """
 
