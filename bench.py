@@ -408,6 +408,20 @@ def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
     return res
 
 
+def geometry_summary(geoms, geoms8):
+    """Compact per-geometry rows for the end of the JSON line: workload,
+    µs per layer, live-band GB/s, fraction of the HBM peak, splits."""
+    if not geoms:
+        return None
+
+    def rows(g):
+        return [[name, round(r["us_per_layer"], 2), round(r["live_GBps"], 1), round(r["frac_of_peak"], 3),
+                 r["num_splits"]] for name, r in g.items()]
+
+    return {"cols": ["workload", "us_per_layer", "live_GBps", "frac_of_peak", "splits"],
+            "bf16": rows(geoms), "e4m3": rows(geoms8) if geoms8 else None}
+
+
 def allocation_independence(steps, stream, device, caps=(4096, 32768, 131072)):
     """Gemma global MQA at len 4096 with the cache allocated at several
     capacities: the time must not grow with the allocation (the page's 537 MB
@@ -573,6 +587,9 @@ def main():
         "geometries": geoms,
         "geometries_e4m3": geoms8,
         "allocation_independence": alloc,
+        # last, so a reader that keeps only the end of the line still has
+        # every geometry: [workload, us/layer, live GB/s, fraction of peak, splits]
+        "geometry_summary": geometry_summary(geoms, geoms8),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

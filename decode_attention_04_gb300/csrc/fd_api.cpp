@@ -351,7 +351,10 @@ int get_workspace(int device, cudaStream_t stream, size_t need, void** ptr) {
   }
   void* p = nullptr;
   if (cudaMalloc(&p, need) != cudaSuccess) return FD_ERR_CUDA;
-  if (cudaMemset(p, 0, need) != cudaSuccess) {  // the counters must start at zero
+  // The counters must start at zero: clear on the call's stream, ahead of the
+  // call's kernels (a plain cudaMemset would run on the legacy stream, which a
+  // non-blocking stream is not ordered with).
+  if (cudaMemsetAsync(p, 0, need, stream) != cudaSuccess) {
     cudaFree(p);
     return FD_ERR_CUDA;
   }
@@ -594,6 +597,7 @@ int fd_get_device_error(fd_stream_t stream, unsigned int* err) {
 }
 
 void fd_release(void) {
+  fd::noalloc_forget();
   std::lock_guard<std::mutex> lk(g_mu);
   for (auto& kv : g_ws) {
     if (kv.second.ptr) {

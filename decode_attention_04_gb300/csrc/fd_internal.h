@@ -68,4 +68,8 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);
 // Read and clear the device error word of the current device.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err);
 
+// fd_decode_attn_noalloc (fd_noalloc.cu): forget each device's scratch set-up,
+// so the next call clears the scratch again.
+void noalloc_forget();
+
 }  // namespace fd

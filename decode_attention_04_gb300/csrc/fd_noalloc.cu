@@ -17,17 +17,22 @@
 // never handed to a kernel: the device address comes from
 // cudaGetSymbolAddress, taken once per device with that device current.
 //
-// The scratch starts with a fixed 64 KB region that holds only split counters
-// (one per (sequence, KV head), up to 16384 of them), then the partials. Each
-// call hands fd_decode_attn_ex a workspace that begins inside that region so
-// that its counters end exactly where the region ends: partials of one shape
-// can then never land on another shape's counters. The set-up of a device
-// clears the whole array once; every completed call leaves its counters at
-// zero again, and every partial a call reads was written earlier in the same
-// call, so nothing is cleared between calls although each call finds the
-// previous call's contents there. All calls on a device share the
-// one array, so calls that overlap on the GPU (on different streams, or from
-// different threads) race on it and must be serialised by the caller.
+// The scratch starts with a fixed 64 KB region that holds only the counters
+// a plan keeps at the head of its workspace (one split counter per (sequence,
+// KV head), plus a work counter for a persistent grid), then the partials.
+// Each call hands fd_decode_attn_ex a workspace that begins inside that region
+// so that its counters end exactly where the region ends: partials of one
+// shape can then never land on another shape's counters. The set-up of a
+// device clears the whole array once, on the caller's stream, and waits for
+// that stream, so the clear has finished before any later call on any stream
+// runs; every completed call leaves its counters at zero again, and every
+// partial a call reads was written earlier in the same call, so nothing is
+// cleared between calls although each call finds the previous call's contents
+// there. A call that fails part-way (a launch error, or a device wait that
+// gave up) may leave a counter non-zero: fd_release makes the next call on
+// each device run the set-up, and so the clear, again. All calls on a device
+// share the one array, so calls that overlap on the GPU (on different streams,
+// or from different threads) race on it and must be serialised by the caller.
 
 #include <map>
 #include <mutex>
@@ -35,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include "fd_decode_attn.h"
+#include "fd_internal.h"
 
 namespace {
 
@@ -47,9 +53,9 @@ std::map<int, void*> g_scratch_addr;  // device -> device address of the array
 
 // Device address of the scratch array on `device`, which must be the current
 // device. The first call for a device performs the lookup (and, with lazy
-// module loading, loads this module on that device) and clears the array;
-// later calls return the cached address.
-int scratch_address(int device, void** ptr) {
+// module loading, loads this module on that device), clears the array on
+// `stream` and waits for that stream; later calls return the cached address.
+int scratch_address(int device, cudaStream_t stream, void** ptr) {
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   auto it = g_scratch_addr.find(device);
   if (it != g_scratch_addr.end()) {
@@ -58,15 +64,29 @@ int scratch_address(int device, void** ptr) {
   }
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FD_ERR_CUDA;
-  // The split counters at the head of the scratch must start at zero (every
-  // completed call leaves them zero again); clear the whole array once.
-  if (cudaMemset(p, 0, FD_NOALLOC_SCRATCH_BYTES) != cudaSuccess) return FD_ERR_CUDA;
+  // The counters at the head of the scratch must start at zero (every
+  // completed call leaves them zero again). The clear goes on the caller's
+  // stream, ahead of this call's kernels, and the wait makes it finished for
+  // calls on every other stream too.
+  if (cudaMemsetAsync(p, 0, FD_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) return FD_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FD_ERR_CUDA;
   g_scratch_addr[device] = p;
   *ptr = p;
   return FD_OK;
 }
 
 }  // namespace
+
+namespace fd {
+
+// Forget every device's set-up, so the next call on each device looks the
+// address up and clears the array again (called by fd_release).
+void noalloc_forget() {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  g_scratch_addr.clear();
+}
+
+}  // namespace fd
 
 extern "C" int fd_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out,
                                       const int* lens, int B, int NH, int NKV, int HS, int capacity,
@@ -88,7 +108,7 @@ extern "C" int fd_decode_attn_noalloc(const void* q, const void* k_cache, const 
   void* ws = nullptr;
   if (plan.workspace_bytes > 0) {
     void* base = nullptr;
-    rc = scratch_address(device, &base);
+    rc = scratch_address(device, reinterpret_cast<cudaStream_t>(stream), &base);
     if (rc != FD_OK) return rc;
     ws = static_cast<unsigned char*>(base) + (kCounterRegion - counters);
   }

@@ -334,17 +334,24 @@ int fd_decode_attn_fp8_ex(const fd_plan_t* plan, void* workspace, size_t workspa
  * counterpart on the pages; it is an addition of this library.
  *   - Same arguments, layouts and conventions as fd_decode_attn; the plan is
  *     made for the current device with max_len <= 0.
- *   - The array holds split counters for up to 16384 (sequence, KV head)
- *     pairs in its first 64 KB and partials in the rest. A shape whose plan
- *     needs more (B * NKV > 16384, or more than 32 MiB - 64 KB of partials)
- *     is rejected with FD_ERR_SCRATCH_LIMIT before anything is launched
- *     (fd_plan + fd_workspace_bytes tell in advance).
+ *   - The array holds, in its first 64 KB, the counters a plan keeps at the
+ *     head of its workspace (plan->workspace_zero_bytes: one 32-bit split
+ *     counter per (sequence, KV head), rounded up to 256 bytes), and the
+ *     partials in the rest. A shape whose plan needs more
+ *     (workspace_zero_bytes > 64 KB, i.e. B * NKV > 16384, or more than
+ *     32 MiB - 64 KB of partials) is rejected with FD_ERR_SCRATCH_LIMIT
+ *     before anything is launched (fd_plan + fd_workspace_bytes tell in
+ *     advance).
  *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress), clears the array (cudaMemset) and caches
- *     the address; make that first call before any stream capture.
+ *     device (cudaGetSymbolAddress), clears the array with cudaMemsetAsync on
+ *     `stream`, waits for `stream` (once), and caches the address; make that
+ *     first call before any stream capture.
  *   - All calls on a device share the one array and each finds the previous
  *     call's contents in it. The counters must start at zero: the device's
  *     set-up clears the array once and every completed call leaves them zero.
+ *     A call that returned FD_ERR_CUDA, or after which fd_get_device_error
+ *     reported FD_DEVERR_WAIT_TIMEOUT, may leave a counter non-zero: call
+ *     fd_release, and the next call on each device clears the array again.
  *     Calls that overlap on the GPU - other streams, other threads - race on
  *     it: the caller must serialise them.
  * Errors: every FD_ERR_* code.
@@ -361,8 +368,10 @@ int fd_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cac
  */
 int fd_get_device_error(fd_stream_t stream, unsigned int* err);
 
-/* fd_release: free the library-owned workspaces of every device. Not
- * thread-safe against concurrent fd_decode_attn calls. */
+/* fd_release: free the library-owned workspaces of every device, and make
+ * the next fd_decode_attn_noalloc call on each device clear its scratch array
+ * again (the recovery step after a failed call). Not thread-safe against
+ * concurrent calls of the library. */
 void fd_release(void);
 
 /* fd_strerror: static, human-readable text for an FD_* status code. */

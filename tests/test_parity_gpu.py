@@ -14,7 +14,7 @@ import torch
 
 import decode_attention_04_gb300 as fd
 from decode_attention_04_gb300.inputs import WORKLOADS, Workload, make_inputs
-from harness import check, oracle_ref, run
+from harness import Guarded, check, oracle_ref, run
 
 pytestmark = pytest.mark.gpu
 
@@ -205,13 +205,28 @@ def test_library_workspace_entry_equals_explicit_and_graph_replay():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out_g.view(torch.int16), out.view(torch.int16))
-    # lens live on the device: a replay sees new lengths
-    ld.fill_(3000)
-    g.replay()
-    torch.cuda.synchronize()
-    lens2 = torch.tensor([3000], dtype=torch.int32)
-    ref2 = oracle_ref(w, q, k, v, lens2)
-    assert np.abs(out_g.cpu().double().numpy() - ref2).max() <= 2e-2  # bf16 output
+    # lens live on the device: a replay sees new lengths. The same capture
+    # through fd_decode_attn_ex with the fp32 copy, checked against the
+    # oracle at the full tolerance after each replay.
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    ws = torch.zeros(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    o16 = Guarded(w.B * w.NH * w.HS * 2, dev, fill=0xFF)
+    o32 = Guarded(w.B * w.NH * w.HS * 4, dev, fill=0xFF)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        fd.fd_decode_attn_ex(plan, ws, plan.workspace_bytes, o32.ptr(), qd, kd, vd, o16.ptr(), ld, w.B, w.NH,
+                             w.NKV, w.HS, w.capacity, w.window, w.scale)
+    for new_len in (3000, 1024, 700, 5000):
+        ld.fill_(new_len)
+        g.replay()
+        g2.replay()
+        torch.cuda.synchronize()
+        res2 = dict(out=o16.view(torch.bfloat16, (w.B, w.NH, w.HS)).cpu(),
+                    out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(), counters_zero=True,
+                    canaries=o16.canaries_intact() and o32.canaries_intact())
+        ref2 = oracle_ref(w, q, k, v, torch.tensor([new_len], dtype=torch.int32))
+        check(res2, ref2, what=f"graph replay with len {new_len}")
+        assert torch.equal(out_g.cpu().view(torch.int16), res2["out"].view(torch.int16))
 
 
 def test_device_error_word_reports_repaired_lengths():
