@@ -15,9 +15,11 @@ Metric: live-band KV GB/s = sum over layers and sequences of
 band_b * NKV * HS * 2 (K and V) * 2 bytes, divided by the step time, and the
 same time as microseconds per layer. Device time comes from CUDA events around
 CUDA-graph replays of the step; e2e repeats the step through the public call
-(fd_decode_attn via the Python binding) with each step's queries and lengths
-copied from pinned host memory and the outputs copied back inside the timed
-region.
+(fd_decode_attn_ex via the Python binding, with the step's plan and
+workspace) with each step's queries and lengths copied from pinned host memory
+and the outputs copied back inside the timed region. The plan is made once per
+geometry, as a decode loop makes it: for the whole cache, with the step's
+shortest length as its lower bound (fd_plan_min_len; --no-min-len drops it).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
 """
@@ -165,7 +167,7 @@ class Step:
     """L layers of one geometry resident on the device; kv = "bf16" or "e4m3"
     (E4M3 codes with per-(sequence, KV head) scales: half the live bytes)."""
 
-    def __init__(self, w, layers, device, seed_base=0, kv="bf16", path=0):
+    def __init__(self, w, layers, device, seed_base=0, kv="bf16", path=0, min_len=True):
         from decode_attention_04_gb300.inputs import draw_lens, make_inputs, make_inputs_fp8
 
         self.w = w
@@ -187,46 +189,36 @@ class Step:
         self.lens = self.lens_h.to(device)
         self.out = [torch.empty_like(x) for x in self.q]
         self.live = live_band_bytes(w, self.lens_h) // (2 if kv == "e4m3" else 1)
-        # a forced kernel family runs through the explicit-workspace call
-        self.path = path
-        self.forced = None
+        # One plan for the step, made the way a decode loop makes it: for the
+        # cache's whole capacity (max_len 0), with the step's shortest length
+        # as the lower bound on every length (decode lengths only grow, so it
+        # holds for every later replay of a captured step); a forced kernel
+        # family overrides the plan's. One workspace serves the layers in turn.
+        import decode_attention_04_gb300 as fd
+        kvt = fd.FD_KV_E4M3 if kv == "e4m3" else fd.FD_KV_BF16
+        self.the_plan = fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, kv_dtype=kvt)
         if path:
-            import decode_attention_04_gb300 as fd
-            self.forced = self.plan()
-            fd.fd_plan_override(self.forced, 0, path)
-            self.ws = torch.zeros(max(16, self.forced.workspace_bytes), dtype=torch.uint8, device=device)
+            fd.fd_plan_override(self.the_plan, 0, path)
+        if min_len:
+            fd.fd_plan_min_len(self.the_plan, int(self.lens_h.min().item()))
+        self.ws = torch.zeros(max(16, self.the_plan.workspace_bytes), dtype=torch.uint8, device=device)
 
     def plan(self):
-        import decode_attention_04_gb300 as fd
-        if getattr(self, "forced", None) is not None:
-            return self.forced
-        w = self.w
-        kv = fd.FD_KV_E4M3 if self.kv == "e4m3" else fd.FD_KV_BF16
-        return fd.fd_plan_kv(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, kv_dtype=kv)
+        return self.the_plan
 
     def run(self, stream=None):
+        """The step: one fd_decode_attn_ex (or _fp8_ex) call per layer."""
         import decode_attention_04_gb300 as fd
-        w = self.w
-        if self.forced is not None:
-            p = self.forced
-            for i in range(self.L):
-                if self.kv == "e4m3":
-                    fd.fd_decode_attn_fp8_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
-                                             self.ks[i], self.vs[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
-                                             w.capacity, w.window, w.scale, stream)
-                else:
-                    fd.fd_decode_attn_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
-                                         self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
-                                         w.scale, stream)
-            return
-        if self.kv == "e4m3":
-            for i in range(self.L):
-                fd.fd_decode_attn_fp8(self.q[i], self.k[i], self.v[i], self.ks[i], self.vs[i], self.out[i],
-                                      self.lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale, stream)
-            return
+        w, p = self.w, self.the_plan
         for i in range(self.L):
-            fd.fd_decode_attn(self.q[i], self.k[i], self.v[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
-                              w.capacity, w.window, w.scale, stream)
+            if self.kv == "e4m3":
+                fd.fd_decode_attn_fp8_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
+                                         self.ks[i], self.vs[i], self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS,
+                                         w.capacity, w.window, w.scale, stream)
+            else:
+                fd.fd_decode_attn_ex(p, self.ws, p.workspace_bytes, None, self.q[i], self.k[i], self.v[i],
+                                     self.out[i], self.lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window,
+                                     w.scale, stream)
 
 
 def time_graph(step: Step, steps: int, warmup: int, stream, bracket=None):
@@ -385,12 +377,12 @@ def cpu_oracle_sample(w, step: Step, budget_s: float = 1.5):
     return out
 
 
-def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16"):
+def run_geometry(w, steps, warmup, stream, device, peak, kv="bf16", min_len=True):
     from decode_attention_04_gb300.inputs import draw_lens
     lens = draw_lens(w)
     live = live_band_bytes(w, lens)
     L = layers_for(w, live)
-    st = Step(w, L, device, kv=kv)
+    st = Step(w, L, device, kv=kv, min_len=min_len)
     ms, _ = time_graph(st, steps, warmup, stream)
     t = statistics.median(ms)
     plan = st.plan()
@@ -422,7 +414,7 @@ def geometry_summary(geoms, geoms8):
             "bf16": rows(geoms), "e4m3": rows(geoms8) if geoms8 else None}
 
 
-def allocation_independence(steps, stream, device, caps=(4096, 32768, 131072)):
+def allocation_independence(steps, stream, device, caps=(4096, 32768, 131072), min_len=True):
     """Gemma global MQA at len 4096 with the cache allocated at several
     capacities: the time must not grow with the allocation (the page's 537 MB
     of whole-allocation reads was the bug this op fixes)."""
@@ -433,7 +425,7 @@ def allocation_independence(steps, stream, device, caps=(4096, 32768, 131072)):
     for cap in caps:
         w = replace(base, name=f"mqa_len4096_cap{cap}", capacity=cap)
         L = 32  # 32 x 8.4 MB live > 2 x L2
-        st = Step(w, L, device)
+        st = Step(w, L, device, min_len=min_len)
         ms, g = time_graph(st, steps, 3, stream)
         out[str(cap)] = {"us_per_layer": statistics.median(ms) * 1e3 / L, "num_splits": st.plan().num_splits}
         del st, g
@@ -450,6 +442,10 @@ def main():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--no-geometries", action="store_true", help="skip the per-geometry table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-min-len", action="store_true",
+                    help="plans without the lengths' lower bound (nothing read before the lengths)")
+    ap.add_argument("--only", default="", help="comma-separated geometries for the per-geometry tables")
+    ap.add_argument("--no-e4m3", action="store_true", help="skip the E4M3 per-geometry table")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling mode: N plain fd_decode_attn calls on one layer of --workload, then exit")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "e4m3"],
@@ -468,7 +464,7 @@ def main():
     if args.impl == "reference":
         return reference_arm(args, w, rank, world)
     if args.profile_calls:
-        return profile_calls(w, args.profile_calls, args.kv, args.path)
+        return profile_calls(w, args.profile_calls, args.kv, args.path, not args.no_min_len)
 
     import decode_attention_04_gb300 as fd
     from decode_attention_04_gb300 import build as libbuild
@@ -485,9 +481,10 @@ def main():
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.Stream(device)
 
-    step = Step(w, layers_for(w, 0), device)
+    use_min_len = not args.no_min_len
+    step = Step(w, layers_for(w, 0), device, min_len=use_min_len)
     L = step.L
-    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    plan = step.plan()
     launches_per_call = kernels_per_call(plan)
 
     # ---- device-timed steps (graph replay), clocks sampled during the region
@@ -530,11 +527,17 @@ def main():
         del step
         torch.cuda.empty_cache()
         geoms, geoms8 = {}, {}
-        for name, gw in WORKLOADS.items():
-            geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak)
-        for name, gw in WORKLOADS.items():
-            geoms8[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak, kv="e4m3")
-        alloc = allocation_independence(max(10, min(args.steps, 30)), stream, device)
+        only = [x for x in args.only.split(",") if x]
+        todo = {n: g for n, g in WORKLOADS.items() if not only or n in only}
+        for name, gw in todo.items():
+            geoms[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak,
+                                       min_len=use_min_len)
+        if not args.no_e4m3:
+            for name, gw in todo.items():
+                geoms8[name] = run_geometry(gw, max(10, min(args.steps, 30)), 3, stream, device, peak, kv="e4m3",
+                                            min_len=use_min_len)
+        if not only:
+            alloc = allocation_independence(max(10, min(args.steps, 30)), stream, device, min_len=use_min_len)
 
     traffic = None
     tf = ROOT / "profiles" / "traffic.txt"
@@ -567,6 +570,8 @@ def main():
             "num_splits": plan.num_splits,
             "l2": f"inputs larger than L2: {L} layers x {live / 1e6:.1f} MB live band = {L * live / 1e6:.0f} MB per step vs 129 MB L2",
             "timing": "CUDA events around CUDA-graph replays of the step, on the launching stream",
+            "plan": {"num_splits": plan.num_splits, "min_len": plan.min_len, "path": plan.path,
+                     "call": "fd_decode_attn_ex, one plan and workspace for the step"},
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
@@ -598,12 +603,12 @@ def main():
     return 0
 
 
-def profile_calls(w, n, kv="bf16", path=0):
+def profile_calls(w, n, kv="bf16", path=0, min_len=True):
     """N plain calls on one layer (for ncu launch lists and captures)."""
     from decode_attention_04_gb300 import build as libbuild
     libbuild.build()
     device = torch.device("cuda", 0)
-    st = Step(w, 1, device, kv=kv, path=path)
+    st = Step(w, 1, device, kv=kv, path=path, min_len=min_len)
     for _ in range(n):
         st.run()
     torch.cuda.synchronize()

@@ -45,6 +45,7 @@ FD_NOALLOC_SCRATCH_BYTES = 32 << 20
 FD_DEVERR_LEN_NEGATIVE = 1 << 0
 FD_DEVERR_LEN_CLAMPED = 1 << 1
 FD_DEVERR_WAIT_TIMEOUT = 1 << 2
+FD_DEVERR_MIN_LEN = 1 << 3
 
 FD_PATH_AUTO = 0
 FD_PATH_SIMT = 1
@@ -55,9 +56,10 @@ FD_KV_BF16 = 0
 FD_KV_E4M3 = 1
 
 EXPORTED = ["fd_plan", "fd_plan_sms", "fd_plan_kv", "fd_plan_sms_kv", "fd_plan_override", "fd_plan_persistent",
-            "fd_workspace_bytes",
+            "fd_plan_min_len", "fd_workspace_bytes",
             "fd_decode_attn", "fd_decode_attn_ex", "fd_decode_attn_fp8", "fd_decode_attn_fp8_ex",
-            "fd_decode_attn_noalloc", "fd_get_device_error", "fd_release", "fd_strerror", "fd_version"]
+            "fd_decode_attn_noalloc", "fd_debug_withhold_copies", "fd_get_device_error", "fd_release",
+            "fd_strerror", "fd_version"]
 
 
 class fd_plan_t(ctypes.Structure):
@@ -75,6 +77,7 @@ class fd_plan_t(ctypes.Structure):
         ("kv_dtype", ctypes.c_int),
         ("consumer_warps", ctypes.c_int),
         ("persistent", ctypes.c_int),
+        ("min_len", ctypes.c_int),
         ("workspace_bytes", ctypes.c_size_t),
         ("workspace_zero_bytes", ctypes.c_size_t),
         ("B", ctypes.c_int),
@@ -117,6 +120,8 @@ def load_library(path: Path | str | None = None):
         "fd_plan_sms_kv": (ci, [ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, planp]),
         "fd_plan_override": (ci, [planp, ci, ci, ci, ci]),
         "fd_plan_persistent": (ci, [planp, ci]),
+        "fd_plan_min_len": (ci, [planp, ci]),
+        "fd_debug_withhold_copies": (ci, [ci, ctypes.c_ulonglong]),
         "fd_workspace_bytes": (sz, [planp]),
         "fd_decode_attn": (ci, [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, vp]),
         "fd_decode_attn_ex": (ci, [planp, vp, sz, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci,
@@ -215,6 +220,21 @@ def fd_plan_persistent(plan: fd_plan_t, persistent: int = 1) -> fd_plan_t:
     return plan
 
 
+def fd_plan_min_len(plan: fd_plan_t, min_len: int) -> fd_plan_t:
+    """Record the caller's lower bound on every len_b (tiles of slots that any
+    such length makes live may then be read before the lengths arrive)."""
+    _check(load_library().fd_plan_min_len(ctypes.byref(plan), int(min_len)), "fd_plan_min_len")
+    return plan
+
+
+def fd_debug_withhold_copies(withhold_tile: int, wait_limit_ns: int = 0) -> None:
+    """Test hook of the bounded waits: split blocks issue no copies from
+    their tile `withhold_tile` on (< 0: off), and waits give up after
+    `wait_limit_ns` (0: the default, about one second)."""
+    _check(load_library().fd_debug_withhold_copies(int(withhold_tile), int(wait_limit_ns)),
+           "fd_debug_withhold_copies")
+
+
 def fd_workspace_bytes(plan: fd_plan_t) -> int:
     return load_library().fd_workspace_bytes(ctypes.byref(plan))
 
@@ -254,11 +274,17 @@ def fd_decode_attn(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, win
 
 def fd_decode_attn_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k_cache, v_cache, out, lens,
                       B, NH, NKV, HS, capacity, window, scale, stream=None) -> None:
-    _check(load_library().fd_decode_attn_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
-                                            _ptr(out_f32), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
-                                            _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
-                                            _stream(stream)),
-           "fd_decode_attn_ex")
+    f = _fast()
+    if f is not None:
+        rc = f.decode_attn_ex(ctypes.addressof(plan), _ptr(workspace) or 0, int(workspace_bytes), _ptr(out_f32) or 0,
+                              _ptr(q) or 0, _ptr(k_cache) or 0, _ptr(v_cache) or 0, _ptr(out) or 0, _ptr(lens) or 0,
+                              B, NH, NKV, HS, capacity, window, float(scale), _stream(stream) or 0)
+    else:
+        rc = load_library().fd_decode_attn_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
+                                              _ptr(out_f32), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out),
+                                              _ptr(lens), B, NH, NKV, HS, capacity, window, float(scale),
+                                              _stream(stream))
+    _check(rc, "fd_decode_attn_ex")
 
 
 def fd_decode_attn_fp8(q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, capacity, window, scale,
@@ -277,11 +303,18 @@ def fd_decode_attn_fp8(q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, c
 
 def fd_decode_attn_fp8_ex(plan: fd_plan_t, workspace, workspace_bytes, out_f32, q, k8, v8, k_scale, v_scale, out,
                           lens, B, NH, NKV, HS, capacity, window, scale, stream=None) -> None:
-    _check(load_library().fd_decode_attn_fp8_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
-                                                _ptr(out_f32), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale),
-                                                _ptr(v_scale), _ptr(out), _ptr(lens), B, NH, NKV, HS, capacity,
-                                                window, float(scale), _stream(stream)),
-           "fd_decode_attn_fp8_ex")
+    f = _fast()
+    if f is not None:
+        rc = f.decode_attn_fp8_ex(ctypes.addressof(plan), _ptr(workspace) or 0, int(workspace_bytes),
+                                  _ptr(out_f32) or 0, _ptr(q) or 0, _ptr(k8) or 0, _ptr(v8) or 0, _ptr(k_scale) or 0,
+                                  _ptr(v_scale) or 0, _ptr(out) or 0, _ptr(lens) or 0, B, NH, NKV, HS, capacity,
+                                  window, float(scale), _stream(stream) or 0)
+    else:
+        rc = load_library().fd_decode_attn_fp8_ex(ctypes.byref(plan), _ptr(workspace), int(workspace_bytes),
+                                                  _ptr(out_f32), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                                                  _ptr(v_scale), _ptr(out), _ptr(lens), B, NH, NKV, HS, capacity,
+                                                  window, float(scale), _stream(stream))
+    _check(rc, "fd_decode_attn_fp8_ex")
 
 
 def fd_decode_attn_noalloc(q, k_cache, v_cache, out, lens, B, NH, NKV, HS, capacity, window, scale,

@@ -2,6 +2,8 @@
 // workspace, and the exported C entry points declared in fd_decode_attn.h.
 
 #include <algorithm>
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -19,6 +21,10 @@
 namespace {
 
 constexpr int kMaxGroup = 16;
+
+// Test hook (fd_debug_withhold_copies): the tile index from which split blocks
+// issue no copies; INT_MAX: off.
+std::atomic<int> g_withhold_tile{INT_MAX};
 
 bool supported_hs(int HS) { return HS == 64 || HS == 128 || HS == 256 || HS == 512; }
 
@@ -418,6 +424,8 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.cluster = plan.cluster;
   a.granule = plan.granule;
   a.path = plan.path;
+  a.min_len = plan.min_len;
+  a.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
   a.scale_log2 = scale * 1.4426950408889634f;
   return fd::launch_decode(a, stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
@@ -497,6 +505,12 @@ int fd_plan_persistent(fd_plan_t* plan, int persistent) {
   return FD_OK;
 }
 
+int fd_plan_min_len(fd_plan_t* plan, int min_len) {
+  if (!plan || min_len < 0) return FD_ERR_INVALID_ARG;
+  plan->min_len = min_len;
+  return FD_OK;
+}
+
 size_t fd_workspace_bytes(const fd_plan_t* plan) { return plan ? ws_total(*plan) : 0; }
 
 }  // extern "C"
@@ -515,6 +529,7 @@ int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int 
   if (plan->num_splits < 1 || !valid_path(*plan) || plan->granule < 1 || !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
       (plan->fused && !fused_rule_allowed(*plan)))
     return FD_ERR_INVALID_ARG;
+  if (plan->min_len < 0) return FD_ERR_INVALID_ARG;
   if (plan->persistent < 0 ||
       (plan->persistent > 0 && (!persistent_allowed(*plan) || plan->persistent > work_items(*plan))))
     return FD_ERR_INVALID_ARG;
@@ -587,6 +602,14 @@ int fd_decode_attn_fp8(const void* q, const void* k8, const void* v8, const floa
                        float scale, fd_stream_t stream) {
   return run_auto(FD_KV_E4M3, q, k8, v8, k_scale, v_scale, out, lens, B, NH, NKV, HS, capacity, window, scale,
                   stream);
+}
+
+int fd_debug_withhold_copies(int withhold_tile, unsigned long long wait_limit_ns) {
+  const bool on = withhold_tile >= 0;
+  const unsigned long long ns = on ? wait_limit_ns : 0;
+  if (fd::set_wait_limit(ns) != cudaSuccess || fd::set_wait_limit_umma(ns) != cudaSuccess) return FD_ERR_CUDA;
+  g_withhold_tile.store(on ? withhold_tile : INT_MAX, std::memory_order_relaxed);
+  return FD_OK;
 }
 
 int fd_get_device_error(fd_stream_t stream, unsigned int* err) {

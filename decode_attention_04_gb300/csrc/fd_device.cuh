@@ -8,6 +8,10 @@
 
 __device__ unsigned int g_device_error;
 
+// Wall-time limit of every bounded wait, nanoseconds (about one second; the
+// host may shorten it for a test of the timeout path).
+__device__ unsigned long long g_wait_limit_ns = 1000000000ull;
+
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // Live band of sequence b: positions [lo, lo + band). Reports repaired
@@ -108,19 +112,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait: gives up after about one second of wall time, raises
-// FD_DEVERR_WAIT_TIMEOUT and returns false. `failed` is sticky per thread, so
-// after one timeout every later wait of that thread returns at once and the
-// kernel runs to its end; no wait in this library can hang the GPU.
-constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
-
+// Bounded wait: gives up after g_wait_limit_ns of wall time (about one
+// second), raises FD_DEVERR_WAIT_TIMEOUT and returns false. `failed` is sticky
+// per thread, so after one timeout every later wait of that thread returns at
+// once and the kernel runs to its end; no wait in this library can hang the
+// GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& failed) {
   if (failed) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = g_wait_limit_ns;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit) break;
   }
   failed = true;
   atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);

@@ -38,6 +38,10 @@ struct LaunchArgs {
   int tile_stride;          // > 0: the split kernel dealt T = tile_stride position tiles to the splits in
                             // turn (bands of slots [0, band)); 0: consecutive chunks (set at launch)
   int path;                 // FD_PATH_SIMT / FD_PATH_TC / FD_PATH_UMMA
+  int min_len;              // every lens[b] >= min_len (the caller's bound; 0: none): tiles of slots
+                            // [0, min(min_len, capacity)) are live before the lengths are read
+  int withhold_tile;        // test hook: tensor-core split blocks issue no copies from this tile of
+                            // theirs on (a huge value: off)
   float scale_log2;         // scale * log2(e)
 };
 
@@ -67,6 +71,12 @@ cudaError_t launch_decode(const LaunchArgs& a, cudaStream_t stream);
 
 // Read and clear the device error word of the current device.
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err);
+
+// Wall-time limit of the kernels' bounded waits on the current device, in
+// nanoseconds (0: the default, about one second); one setter per
+// translation unit that holds kernels.
+cudaError_t set_wait_limit(unsigned long long ns);
+cudaError_t set_wait_limit_umma(unsigned long long ns);
 
 // fd_decode_attn_noalloc (fd_noalloc.cu): forget each device's scratch set-up,
 // so the next call clears the scratch again.

@@ -360,6 +360,19 @@ __device__ __forceinline__ void produce_tile(const LaunchArgs& a, const unsigned
   }
 }
 
+// A producer warp's last step: wait (bounded, with its own failure flag) for
+// the last phase it issued into each stage of the ring, so no copy of this
+// block is still in flight when the block exits. Earlier phases of a stage
+// completed before that stage was issued again, and only the producers
+// arrive on the full barriers, so the last issued phase is the last phase.
+template <class C>
+__device__ __forceinline__ void producer_drain(uint32_t full0, uint32_t st_issued, uint32_t st_par) {
+  bool dfail = false;
+#pragma unroll
+  for (int st = 0; st < C::NSTAGE; ++st)
+    if ((st_issued >> st) & 1u) mbar_wait(full0 + 8 * st, (st_par >> st) & 1u, dfail);
+}
+
 template <class C, bool PERSIST = false>
 __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -399,28 +412,36 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   // With no window, or a window as long as the cache, a band's slots are
   // [0, band), and the splits take its T-position tiles in turn (split s:
-  // tiles s, s + S, s + 2S, ...), so a split's first tile, slots
-  // [s*T, s*T + T), is known before the length is. A per-split block whose
-  // sequence needs no ordering table asks L2 for that tile while the previous
-  // kernel is still running (a hint only: the copies that use the tile come
-  // after the dependency wait), then, past the wait, issues the tile's copies
-  // at once, into stage 0; if the band turns out not to hold the whole tile,
-  // the stage is waited for and dropped, and the real tiles start at stage 1.
+  // tiles s, s + S, s + 2S, ...), so a split's tiles are known before the
+  // length is, and the tiles of slots [0, min(min_len, capacity)) are live
+  // for every length the caller allows (min_len, the plan's lower bound). A
+  // per-split block whose sequence needs no ordering table asks L2 for its
+  // first such tile while the previous kernel is still running (a hint only:
+  // nothing is read into the block before the dependency wait) and, past the
+  // wait, copies it into stage 0 at once, before its length arrives. Nothing
+  // else is read before the length is known, so only live slots are read.
+  // (If a length breaks the bound, a tile copied early that the band does not
+  // reach is never used: the producers wait for its copies before leaving.)
+  // Measured on GB300 (us per layer; ring / MQA 32k / MQA 4k / Llama tiny):
+  // the first tile requested and copied early 6.14 / 19.7 / 8.88 / 5.08;
+  // the first NSTAGE tiles copied early 6.20 / 19.7 / 9.00 / 5.00; every sure
+  // tile requested from L2 (up to a quarter of L2 over the grid) 6.20 / 21.7
+  // / 9.00 / 5.08 (the requests delay the first tile's copies); nothing
+  // requested, the first tiles copied early 6.66 / 20.1 / 9.06 / 5.25.
+  constexpr int kRowBytesT = C::KV8 ? C::ROWB8 : C::ROWB;
+  constexpr int kTileBytes = C::T * kRowBytesT;  // one tensor's bytes of one tile
   const bool tiled = a.window <= 0 || a.window >= a.capacity;
   const bool len_early = !PERSIST && !lpt_ordered(a);
-  const bool spec = len_early && a.cluster == 1 && tiled;
-  int spec_nv = 0;
-  long long sp0 = 0;
-  if (spec) {
-    sp0 = static_cast<long long>(blockIdx.x) * C::T;
-    spec_nv = static_cast<int>(max(0ll, min(static_cast<long long>(C::T), a.capacity - sp0)));
-    if (spec_nv > 0 && warp >= C::NWC && lane == 0) {
-      constexpr int kRowBytes = C::KV8 ? C::ROWB8 : C::ROWB;
-      const bool is_k = warp == C::NWC;
-      prefetch_l2(producer_src<C>(a, is_k, blockIdx.z, blockIdx.y) + sp0 * kRowBytes,
-                  static_cast<uint32_t>(spec_nv) * kRowBytes);
-    }
+  int n_sure = 0;  // this split's tiles that every allowed length makes live
+  if (len_early && tiled) {
+    const int nt_sure = min(a.min_len, a.capacity) / C::T;
+    const int s0 = static_cast<int>(blockIdx.x);
+    n_sure = nt_sure > s0 ? (nt_sure - s0 + a.num_splits - 1) / a.num_splits : 0;
   }
+  const int n_early = min(min(n_sure, 1), max(0, a.withhold_tile));  // copied before the length is read
+  if (n_sure > 0 && warp >= C::NWC && lane == 0)
+    prefetch_l2(producer_src<C>(a, warp == C::NWC, blockIdx.z, blockIdx.y) +
+                    static_cast<long long>(blockIdx.x) * kTileBytes, kTileBytes);
   // The block's query rows (G consecutive heads, contiguous) do not depend on
   // the length: ask L2 for them too.
   if (len_early && tid == 0)
@@ -434,11 +455,19 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   lpt_table(a, tid, C::THREADS, s_seq);
   __syncthreads();
 
-  if (spec) {
-    if (spec_nv > 0 && warp >= C::NWC) {
-      const bool is_k = warp == C::NWC;
-      produce_tile<C>(a, producer_src<C>(a, is_k, blockIdx.z, blockIdx.y), smem_u32(smem + producer_ring<C>(is_k)),
-                      full0, sp0, spec_nv, lane);
+  // Stage-ring bookkeeping of a producer warp: the stages it has issued copies
+  // into, and the phase parity of each stage's last issue (for the drain).
+  uint32_t st_issued = 0, st_par = 0;
+  if (n_early > 0 && warp >= C::NWC) {
+    const bool is_k = warp == C::NWC;
+    const unsigned char* src = producer_src<C>(a, is_k, blockIdx.z, blockIdx.y);
+    constexpr size_t kStageBytes = C::KV8 ? C::STAGE8_BYTES : C::STAGE_BYTES;
+    const uint32_t ring = smem_u32(smem + producer_ring<C>(is_k));
+    for (int i = 0; i < n_early; ++i) {  // tiles 0 .. n_early - 1 of the split: stages 0 .. n_early - 1
+      produce_tile<C>(a, src, ring + static_cast<uint32_t>(i * kStageBytes), full0 + 8 * i,
+                      (static_cast<long long>(blockIdx.x) + static_cast<long long>(i) * a.num_splits) * C::T, C::T,
+                      lane);
+      st_issued |= 1u << i;
     }
   }
 
@@ -488,8 +517,10 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   const int hbase = kvh * G;
 
   int lo;
-  const int band = band_of(len_early ? len_first : a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0,
-                           &lo);
+  const int len_b = len_early ? len_first : a.lens[b];
+  const bool reporter = s == 0 && kvh == 0 && tid == 0;
+  if (reporter && len_b < a.min_len) atomicOr(&g_device_error, FD_DEVERR_MIN_LEN);
+  const int band = band_of(len_b, a.capacity, a.window, reporter, &lo);
   // This split's tiles: tile i holds positions [tile_pos(i), + tile_nv(i)).
   // Tiled bands (slots [0, band)): tiles s, s + S, ... of the band; other
   // bands: the consecutive positions [lo + s*chunk, ...) cut into tiles. The
@@ -509,11 +540,11 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   };
   const int CS = a.cluster;                 // blocks per cluster along the splits
   const bool direct = S == CS;              // one block / cluster spans every split
-  const bool spec_hit = spec_nv > 0 && ntiles > 0 && tile_nv(0) == spec_nv;  // the speculative tile is tile 0
-  const bool spec_miss = spec_nv > 0 && !spec_hit;                           // stage 0 holds copies to drop
 
   if (ntiles == 0 && CS == 1) {
-    if (spec_miss) mbar_wait(full0, 0, failed);  // no copy may land after the block has left
+    // no copy may land after the block has left (tiles copied early for a
+    // length below the plan's bound)
+    if (!persist && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
     // len == 0: the output row is zero. With one block per band, or with the
     // fused merge (no block of an empty band ever merges), block 0 writes it.
     if (direct || (a.fused && band == 0 && s == 0)) {
@@ -529,7 +560,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   // In a cluster every block, even one with an empty slice (m = -inf, l = 0,
   // O = 0), takes part in the reduction at the end.
-  const int gbase = gnext + (spec_miss ? 1 : 0);  // pipeline tiles of this block's earlier items
+  const int gbase = gnext;  // pipeline tiles of this block's earlier items
   gnext = gbase + ntiles;
 
   const int grp = lane >> 2, t4 = lane & 3;
@@ -552,8 +583,8 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     const unsigned char* src = producer_src<C>(a, is_k, b, kvh);
     constexpr size_t kStageBytes = C::KV8 ? C::STAGE8_BYTES : C::STAGE_BYTES;
     const size_t ring = producer_ring<C>(is_k);
-    for (int i = 0; i < ntiles; ++i) {
-      if (spec_hit && i == 0) continue;  // already in flight in stage 0
+    for (int i = persist ? 0 : n_early; i < ntiles; ++i) {  // tiles [0, n_early) are in flight already
+      if (!persist && i >= a.withhold_tile) break;              // test hook: these copies are never issued
       const int gi = gbase + i;
       const int st = gi % C::NSTAGE;
       if (gi >= C::NSTAGE) mbar_wait(empty0 + 8 * st, ((gi / C::NSTAGE) - 1) & 1, failed);
@@ -562,7 +593,12 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       const long long pbase = tile_pos(i);
       produce_tile<C>(a, src, smem_u32(smem + ring + static_cast<size_t>(st) * kStageBytes), full0 + 8 * st, pbase,
                       nv, lane);
+      st_issued |= 1u << st;
+      st_par = (st_par & ~(1u << st)) | (static_cast<uint32_t>((gi / C::NSTAGE) & 1) << st);
     }
+    // Every copy this warp issued has landed before the block can leave: a
+    // consumer wait that gave up must not leave copies in flight.
+    if (!persist) producer_drain<C>(full0, st_issued, st_par);
   } else {
   // -------------------------------------------------------------- consumers
 
@@ -634,11 +670,6 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
 
   // ldmatrix lane addressing
   const int lrow = lane & 7, lmat = lane >> 3;
-  if (spec_miss) {  // drop the speculative stage: wait for its copies, then free it
-    mbar_wait(full0, 0, failed);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0);
-  }
 
   for (int i = 0; i < ntiles; ++i) {
     const int gi = gbase + i;
@@ -1081,6 +1112,7 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   }
   cluster_sync_all();  // no block leaves while another still reads its shared memory
   }  // work items
+  if (PERSIST && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
 }
 
 // ================================================================ merge kernel
@@ -1104,6 +1136,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArg
   __shared__ float sm[kMergeWarps];
   const int slab = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Dependents are released after the wait, not before: letting the next
+  // split grid become resident while this layer's split grid still streams
+  // cost the small-band ring 0.6 us per layer on GB300 (its early L2
+  // requests compete with this layer's reads), more than it gained on MQA.
   grid_dependency_wait();
   grid_launch_dependents();
   const int len_b = a.lens[b];
@@ -1573,6 +1609,11 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 mgrid(a.HS / kMergeDims, a.NH, a.B);
   return launch_pdl(merge_staged_kernel, mgrid, dim3(kMergeThreads), msmem, stream, 1, a);
+}
+
+cudaError_t set_wait_limit(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : 1000000000ull;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof v);
 }
 
 cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* err) {

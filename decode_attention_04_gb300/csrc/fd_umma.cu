@@ -632,6 +632,11 @@ cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, split_umma_kernel<kUmmaTile>, maps, a);
 }
 
+cudaError_t set_wait_limit_umma(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : 1000000000ull;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof v);
+}
+
 cudaError_t read_and_clear_device_error_umma(unsigned int* err) {
   unsigned int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);

@@ -76,7 +76,9 @@ enum {
 enum {
   FD_DEVERR_LEN_NEGATIVE = 1u << 0,  /* some len_b < 0; treated as 0 */
   FD_DEVERR_LEN_CLAMPED = 1u << 1,   /* no window and len_b > capacity; band clamped */
-  FD_DEVERR_WAIT_TIMEOUT = 1u << 2   /* a pipeline wait gave up; the output is invalid */
+  FD_DEVERR_WAIT_TIMEOUT = 1u << 2,  /* a pipeline wait gave up; the output is invalid */
+  FD_DEVERR_MIN_LEN = 1u << 3        /* some len_b < the plan's min_len: slots outside the live band
+                                        may have been read early (the output is still exact) */
 };
 
 /* KV cache element types (fd_plan_t.kv_dtype). */
@@ -166,6 +168,7 @@ typedef struct {
   int kv_dtype;            /* FD_KV_BF16 or FD_KV_E4M3: the cache type the plan was made for */
   int consumer_warps;      /* MMA warps per split block (2, 4 or 8; 0 on the SIMT path) */
   int persistent;          /* blocks of a persistent split grid (fd_plan_persistent); 0: one block per split */
+  int min_len;             /* caller's lower bound on every len_b (fd_plan_min_len); 0: none */
   size_t workspace_bytes;  /* bytes of workspace fd_decode_attn_ex needs */
   size_t workspace_zero_bytes; /* leading workspace bytes that must be zero before first use */
   /* the shape the plan was made for; fd_decode_attn_ex checks it */
@@ -240,6 +243,26 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
  * not available).
  */
 int fd_plan_persistent(fd_plan_t* plan, int persistent);
+
+/*
+ * fd_plan_min_len: record that every len_b the plan will be used with is at
+ * least min_len (>= 0; 0, the plans' default, promises nothing). The live band
+ * is read only: a split block reads nothing before it has read its sequence's
+ * length, except the tiles of slots that every length >= min_len makes live.
+ * With no window, or a window as long as the cache, the band's slots are
+ * [0, min(len_b, capacity)), so the slots [0, min(min_len, capacity)) are live
+ * for any such length; the tensor-core kernel asks L2 for this split's such
+ * tiles while the previous kernel on the stream still runs, and copies its
+ * first ones as soon as that kernel is done, before its length arrives
+ * ("Hand-Writing Gemma 4 Flash-Decoding + an FP4 Matvec Bonus (Part 2)",
+ * section "One KV head breaks the textbook": reads only the live band, never
+ * the allocation). A decode loop's host knows its lengths, so it can pass the
+ * smallest; a full sliding ring (len_b >= capacity) passes capacity. A length
+ * below the bound still gives the exact result (tiles read early and not in
+ * the band are never used) and raises FD_DEVERR_MIN_LEN.
+ * Errors: FD_ERR_INVALID_ARG (null plan, min_len < 0).
+ */
+int fd_plan_min_len(fd_plan_t* plan, int min_len);
 
 /*
  * fd_workspace_bytes: workspace a plan needs. With P = num_splits / cluster
@@ -359,6 +382,22 @@ int fd_decode_attn_fp8_ex(const fd_plan_t* plan, void* workspace, size_t workspa
 int fd_decode_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, void* out,
                            const int* lens, int B, int NH, int NKV, int HS, int capacity,
                            int window, float scale, fd_stream_t stream);
+
+/*
+ * fd_debug_withhold_copies: a test hook for the bounded waits (no counterpart
+ * on the pages). With withhold_tile >= 0, the tensor-core split blocks of
+ * every later call on any device issue no K/V copies for their tiles from
+ * index withhold_tile on (they never issue those copies, so nothing is left
+ * in flight), the consumer warps' wait for that tile gives up after
+ * wait_limit_ns nanoseconds (0: the default, about one second), the call
+ * completes with an invalid output, and fd_get_device_error reports
+ * FD_DEVERR_WAIT_TIMEOUT; the workspace counters may then be non-zero.
+ * withhold_tile < 0 restores normal operation and the default limit. Sets the
+ * limit on the current device (a synchronous copy); not for use while other
+ * threads call the library.
+ * Errors: FD_ERR_CUDA.
+ */
+int fd_debug_withhold_copies(int withhold_tile, unsigned long long wait_limit_ns);
 
 /*
  * fd_get_device_error: wait for `stream`, then return in *err the OR of the

@@ -44,10 +44,11 @@ class Guarded:
 
 def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len: int = 0,
         poison_ws: bool = True, device="cuda", inputs_on_device=False, scale=None, cluster: int = 0,
-        fused: int = -1, persistent: int = -1):
+        fused: int = -1, persistent: int = -1, min_len: int = 0):
     """One fd_decode_attn_ex call. Returns dict with out (bf16, cpu), out32
     (fp32, cpu), plan, deverr, canaries (bool). persistent: -1 the plan's
-    rule, 0 one block per split, k > 0 a persistent grid of at most k blocks."""
+    rule, 0 one block per split, k > 0 a persistent grid of at most k blocks.
+    min_len: the plan's lower bound on the lengths (fd_plan_min_len)."""
     dev = torch.device(device)
     if inputs_on_device:
         qd, kd, vd, ld = q, k, v, lens.to(dev)
@@ -57,6 +58,8 @@ def run(w, q, k, v, lens, splits: int = 0, path: int = fd.FD_PATH_AUTO, max_len:
     if splits or path or cluster or fused >= 0:
         fd.fd_plan_override(plan, splits, path, cluster, fused)
     set_persistent(plan, persistent)
+    if min_len:
+        fd.fd_plan_min_len(plan, min_len)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)         # NaN-filled: unwritten rows show up
     o32 = Guarded(n * 4, dev, fill=0xFF)
@@ -124,7 +127,8 @@ def oracle_ref(w, q, k, v, lens, rows=None):
 
 
 def run_fp8(w, q, k8, v8, ks, vs, lens, splits: int = 0, max_len: int = 0, device="cuda",
-            inputs_on_device=False, scale=None, cluster: int = 0, fused: int = -1, persistent: int = -1):
+            inputs_on_device=False, scale=None, cluster: int = 0, fused: int = -1, persistent: int = -1,
+            min_len: int = 0):
     """One fd_decode_attn_fp8_ex call over an E4M3 cache (codes k8/v8, scales
     ks/vs); same result dict as run()."""
     dev = torch.device(device)
@@ -136,6 +140,8 @@ def run_fp8(w, q, k8, v8, ks, vs, lens, splits: int = 0, max_len: int = 0, devic
     if splits or cluster or fused >= 0:
         fd.fd_plan_override(plan, splits, 0, cluster, fused)
     set_persistent(plan, persistent)
+    if min_len:
+        fd.fd_plan_min_len(plan, min_len)
     n = w.B * w.NH * w.HS
     o16 = Guarded(n * 2, dev, fill=0xFF)
     o32 = Guarded(n * 4, dev, fill=0xFF)

@@ -396,6 +396,16 @@ def test_compiled_entries_return_the_library_status(lib):
         assert f.decode_attn(*c) == lib.fd_decode_attn(*c) != fd.FD_OK
     c8 = (0, 0, 0, 0, 0, 0, 0, 1, 16, 8, 256, 64, 0, 0.0, 0)
     assert f.decode_attn_fp8(*c8) == lib.fd_decode_attn_fp8(*c8) == fd.FD_ERR_INVALID_ARG
+    # explicit-plan entries: a null plan, and a plan made for another shape
+    tail = (16, 16, 16, 16, 16, 1, 16, 8, 256, 64, 0, 0.0, 0)
+    assert f.decode_attn_ex(0, 0, 0, 0, *tail) == lib.fd_decode_attn_ex(None, None, 0, None, *tail) \
+        == fd.FD_ERR_INVALID_ARG
+    other = _plan(WORKLOADS["llama_tiny"])
+    assert f.decode_attn_ex(ctypes.addressof(other), 0, 0, 0, *tail) == \
+        lib.fd_decode_attn_ex(ctypes.byref(other), None, 0, None, *tail) == fd.FD_ERR_INVALID_ARG
+    tail8 = (16, 16, 16, 16, 16, 16, 16, 1, 16, 8, 256, 64, 0, 0.0, 0)
+    assert f.decode_attn_fp8_ex(0, 0, 0, 0, *tail8) == lib.fd_decode_attn_fp8_ex(None, None, 0, None, *tail8) \
+        == fd.FD_ERR_INVALID_ARG
 
 
 def test_plan_long_bands_with_large_groups_fill_every_slot_once(lib):
@@ -409,3 +419,18 @@ def test_plan_long_bands_with_large_groups_fill_every_slot_once(lib):
     assert _plan(WORKLOADS["gemma_global_mqa_32k"]).num_splits == 152
     one_per_sm = _plan(w, ctas=1)  # no second slot per SM: waves at the 2 MiB bound
     assert -(-w.capacity // one_per_sm.num_splits) * w.HS * 4 <= (2 << 20) + w.HS * 4
+
+
+def test_plan_min_len_recorded_and_checked(lib):
+    """fd_plan_min_len records the caller's lower bound on the lengths; plans
+    start with none; a negative bound is refused; overrides keep it."""
+    w = WORKLOADS["gemma_local_ring"]
+    p = _plan(w)
+    assert p.min_len == 0
+    fd.fd_plan_min_len(p, w.capacity)
+    assert p.min_len == w.capacity
+    fd.fd_plan_override(p, 7, 0, 0, -1)
+    assert p.min_len == w.capacity and p.num_splits == 7
+    assert lib.fd_plan_min_len(ctypes.byref(p), -1) == fd.FD_ERR_INVALID_ARG
+    assert lib.fd_plan_min_len(None, 5) == fd.FD_ERR_INVALID_ARG
+    assert p.min_len == w.capacity
