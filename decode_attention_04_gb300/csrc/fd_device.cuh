@@ -106,6 +106,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (try_wait may suspend the thread for a while
+// when the phase is not complete; a thread that polls several barriers, or
+// only asks whether data has landed yet, must move on at once).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -113,18 +128,26 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait: gives up after g_wait_limit_ns of wall time (about one
-// second), raises FD_DEVERR_WAIT_TIMEOUT and returns false. `failed` is sticky
+// second) past its first 256 polls, raises FD_DEVERR_WAIT_TIMEOUT and returns
+// false. `failed` is sticky
 // per thread, so after one timeout every later wait of that thread returns at
 // once and the kernel runs to its end; no wait in this library can hang the
 // GPU.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& failed) {
   if (failed) return false;
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  const uint64_t limit = g_wait_limit_ns;
-  for (uint32_t i = 1;; ++i) {
+  // The clock is read only every 256 unsuccessful polls (a wait that ends
+  // soon never reads it); the limit counts from the first reading.
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit) break;
+    if ((i & 255u) == 255u) {
+      const uint64_t now = globaltimer_ns();
+      if (i == 255u) {
+        t0 = now;
+      } else if (now - t0 > g_wait_limit_ns) {
+        break;
+      }
+    }
   }
   failed = true;
   atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);

@@ -63,6 +63,7 @@ cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster);
 // The tcgen05 / tensor-memory split kernel (fd_umma.cu): bf16, head dim 512,
 // 8 < G <= 16 query rows per KV head, no window.
 bool umma_shape_ok(int HS, int G, int window);
+int umma_tile_positions();
 cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t read_and_clear_device_error_umma(unsigned int* err);
 

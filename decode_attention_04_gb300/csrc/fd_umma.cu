@@ -3,33 +3,44 @@
 // Flash-Decoding + an FP4 Matvec Bonus (Part 2)", section "One KV head breaks
 // the textbook": one KV head, up to 16 query rows, head dim 512, bf16 cache,
 // no sliding window. Same method as split_tc_kernel (per-split unnormalised
-// (O, m, l) partials, one online-softmax rescale per tile, the same merge
-// kernel), different machinery:
+// (O, m, l) partials merged by the same merge kernels), different machinery:
 //
 //   * With no window the band is [max(0, len - capacity), len), whose slots
-//     are always [0, min(len, capacity)): a split walks slots, not positions,
-//     and a tile never wraps the ring (softmax does not depend on order).
-//   * Warp 0 streams K and V as TMA tiles (128 positions x 64 head dims,
-//     128-byte swizzle, 16 KB) into a ring of 10 chunks; a tile's last, partial
-//     rows come in 8-row boxes.
-//   * Warp 1 owns the tensor memory and issues the MMAs from one thread:
-//     S^T (128 positions x 16 rows, fp32) = K Q^T as 32 MMAs of K = 16 dims,
-//     and O^T (512 dims x 16 rows) += V^T P^T as 4 x 8 MMAs per P half, V read
-//     MN-major from the same TMA tiles, P = hi + lo bf16 (~16 bits of each
-//     weight). The chunks stream as K(0), V(0), K(1), V(1), ...: V(i) lands
-//     while the softmax warps work on S(i); S is double-buffered in TMEM.
-//   * Warps 2-5 read S from tensor memory (one position per thread), take the
-//     row maxima and sums with a halving butterfly (16 shuffles for 16 rows),
-//     write P, rescale O in tensor memory when a row's maximum moved, and
-//     finally store the partial (or the normalised output when S = 1).
+//     are always [0, min(len, capacity)): a split takes the consecutive slots
+//     [s * chunk, (s + 1) * chunk) of that range (the softmax does not depend
+//     on the order of positions), in tiles of 128.
+//   * Warp 0 streams K and warp 1 streams V as TMA boxes (128-byte swizzle,
+//     64 head dims wide) into two separate rings: K in 16 KB chunks (128
+//     positions x 64 dims), V in 32 KB pairs of chunks (128 dims, one P.V
+//     MMA block). Boxes are 128, 64, 32, 16 or 8 rows high, so a tile's rows
+//     are read exactly; the last rows of a slice that do not fill 8 are loaded
+//     by the producer warp's lanes (all of a tile's at once) and stored into
+//     the same swizzled layout. Nothing outside the band is read.
+//   * Warp 2 owns the tensor memory and issues every MMA from one thread, out
+//     of order between two streams: S^T (128 positions x 16 rows, fp32) =
+//     K Q^T as each K chunk lands (4 MMAs of K = 16 dims per chunk, into one
+//     of two S buffers), and O^T (512 dims x 16 rows) += V^T P^T for tile i
+//     once P(i) is ready and each V pair lands (P = hi + lo bf16, ~16 bits of
+//     each weight). The scores of tile i + 1 are therefore computed while the
+//     softmax of tile i runs, and the K stream never waits for V.
+//   * Warps 3-6 read S from tensor memory (one position per thread), take the
+//     tile's row maxima with a halving butterfly (16 shuffles for 16 rows) and
+//     one barrier, and write P. The running maximum moves only when a row's
+//     tile maximum exceeds it by more than 2^8 (then O is rescaled in tensor
+//     memory once the previous P.V is done); otherwise the weights, at most
+//     2^8, are taken against the old maximum, which gives the same softmax.
+//     Row sums stay per thread until the end: one reduction per split.
 //
-// All waits are bounded (fd_device.cuh); the tensor memory is released on
-// every path that allocated it.
+// All waits are bounded (fd_device.cuh); the copy warps wait for their last
+// copies and the MMA warp for its last MMAs before the block leaves, and the
+// tensor memory is released on every path that allocated it.
 
 #include <cuda.h>  // CUtensorMap (descriptor type only; the encoder comes from the runtime)
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "fd_decode_attn.h"
 #include "fd_internal.h"
@@ -40,16 +51,41 @@ namespace {
 #include "fd_device.cuh"
 
 namespace um {
-constexpr int HS = 512;                 // head dim
-constexpr int NQ = 16;                  // query rows per MMA (N); G <= 16, zero rows above G
-constexpr int DC = 64;                  // head dims per chunk: one 128-byte swizzle row
-constexpr int NCH = HS / DC;            // chunks per tensor per tile
-constexpr int TAIL_ROWS = 8;            // box height for a tile's partial rows
-constexpr int NSOFT = 4;                // softmax warps: 2..5, one TMEM lane quarter each
-constexpr int THREADS = (2 + NSOFT) * 32;
-constexpr int ATOM_Q = NQ * 128;        // 16 rows x 128 B: one K-major swizzle column of Q or P
-constexpr int RING_BYTES = 160 * 1024;  // the K/V chunk ring
-constexpr uint32_t TMEM_COLS = 128;     // S[2] at columns 0, 16; O block mb at 32 + 16 mb
+constexpr int HS = 512;                   // head dim
+constexpr int NQ = 16;                    // query rows per MMA (N); G <= 16, zero rows above G
+constexpr int T = 128;                    // positions per tile: the score MMA's M
+constexpr int DC = 64;                    // head dims per chunk: one 128-byte swizzle row
+constexpr int NCH = HS / DC;              // chunks per tensor per tile
+constexpr int CHUNK_BYTES = T * DC * 2;   // one 128-row TMA box: 16 KB
+constexpr int PAIR_BYTES = 2 * CHUNK_BYTES;
+constexpr int NK = 5;                     // K ring: chunks
+constexpr int NVP = 3;                    // V ring: chunk pairs (128 dims: one P.V MMA block)
+constexpr int MAX_TAIL = NCH * 7 * 8 / 32;  // 16-byte tail pieces per lane (at most 7 rows)
+constexpr int NMAP = 5;                   // box heights T, T/2, T/4, T/8, T/16 (= 8)
+constexpr int NSOFT = 4;                  // softmax warps, one TMEM lane quarter each
+constexpr int W_K = 0, W_V = 1, W_MMA = 2, W_SOFT0 = 3;
+constexpr int THREADS = (W_SOFT0 + NSOFT) * 32;
+constexpr int ATOM_Q = NQ * 128;          // 16 rows x 128 B: one K-major swizzle column of Q or P
+constexpr int P_HALF = (T / 64) * ATOM_Q; // T positions of one half (hi or lo)
+constexpr int P_BUF = 2 * P_HALF;         // hi + lo
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + NK * CHUNK_BYTES;
+constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;   // Q: NCH atoms of 16 rows x 64 dims
+constexpr int OFF_P = OFF_Q + NCH * ATOM_Q;       // P: [2 buffers][hi, lo][T / 64 atoms]
+constexpr int OFF_RED = OFF_P + 2 * P_BUF;        // f32 [2][NQ][NSOFT] tile maxima, [NQ][NSOFT] sums
+constexpr int RED_FLOATS = 3 * NQ * NSOFT;
+constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
+// full_k[NK], empty_k[NK], full_v[NVP], empty_v[NVP], s_full[2], s_free[2],
+// p_ready[2], pv_done[2], q_ready, mma_done
+constexpr int NBAR = 2 * NK + 2 * NVP + 8 + 2;
+constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;      // u32: tensor memory base address
+constexpr int SMEM = OFF_TMEM + 16 + 1024;        // + slack to align the base to 1024
+constexpr uint32_t TMEM_COLS = 128;               // S[2] at columns 0, 16; O block mb at 32 + 16 mb
+constexpr float kRescaleLog2 = 8.f;               // the running max moves when a tile's exceeds it by 2^8
+
+static_assert(SMEM <= 227 * 1024, "shared memory");
+static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+static_assert((T >> (NMAP - 1)) == 8, "smallest box: 8 rows (1024 bytes, one swizzle atom)");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5 = 1), A and
 // B bf16 (bits 7-9, 10-12 = 1), A MN-major when bit 15 is set, N / 8 at bits
@@ -58,43 +94,9 @@ constexpr uint32_t idesc_bf16(bool a_mn_major, int M) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          (static_cast<uint32_t>(NQ >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+constexpr uint32_t kIdescQK = idesc_bf16(false, T);   // A = K tile, K-major (dims contiguous), M = 128 positions
 constexpr uint32_t kIdescPV = idesc_bf16(true, 128);  // A = V^T, MN-major (dims contiguous), M = 128 dims
 }  // namespace um
-
-// Tile-dependent layout: T positions per tile (the score MMA's M, 64 or 128).
-// An M = 128 accumulator keeps row r in tensor-memory lane r; an M = 64 one
-// keeps row r in lane 32 (r / 16) + r % 16 (the first 16 lanes of each
-// warp's quarter). P.V always runs with M = 128 head dims.
-template <int T_>
-struct UmmaTile {
-  static constexpr int T = T_;
-  static constexpr int CHUNK_BYTES = T * um::DC * 2;             // one TMA box: T positions x 64 dims
-  static constexpr int NRING = um::RING_BYTES / CHUNK_BYTES;     // even: a V chunk pair never straddles the wrap
-  static constexpr int OFF_RING = 0;
-  static constexpr int OFF_Q = OFF_RING + NRING * CHUNK_BYTES;   // Q: NCH atoms of 16 rows x 64 dims
-  static constexpr int OFF_P = OFF_Q + um::NCH * um::ATOM_Q;     // P: [2 buffers][hi, lo][T / 64 atoms]
-  static constexpr int P_HALF = (T / 64) * um::ATOM_Q;          // T positions of one half (hi or lo)
-  static constexpr int P_BUF = 2 * P_HALF;                       // hi + lo
-  static constexpr int OFF_RED = OFF_P + 2 * P_BUF;              // f32 [2][NQ][NSOFT] row maxima, row sums
-  static constexpr int OFF_BAR = OFF_RED + 2 * um::NQ * um::NSOFT * 4;
-  // full[NRING], empty[NRING], q_ready, s_full[2], p_ready[2], pv_done
-  static constexpr int NBAR = 2 * NRING + 6;
-  static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;            // u32: tensor memory base address
-  static constexpr int SMEM = OFF_TMEM + 16 + 1024;              // + slack to align the base
-  static constexpr int LPQ = T / 4;                              // S rows per warp lane quarter
-  static constexpr uint32_t kIdescQK = um::idesc_bf16(false, T); // A = K tile, K-major (dims contiguous)
-
-  static_assert(T == 64 || T == 128, "score MMA M");
-  static_assert(SMEM <= 227 * 1024, "shared memory");
-  static_assert(NRING % 2 == 0 && NRING >= um::NCH, "ring");
-  static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
-};
-
-// Positions per tile of the kernel the library launches. Measured on GB300
-// (µs per layer, MQA 32k / MQA long at 38 splits): T = 128 26.6 / 189,
-// T = 64 35.2 / 321. A tile's time is mostly its fixed chain (softmax, MMA
-// commits, P.V before the next scores), so halving the tile doubles it.
-constexpr int kUmmaTile = 128;
 
 // Shared-memory matrix descriptor (tcgen05): start address / 16 in bits
 // 0-13, leading-dimension byte offset / 16 in 16-29, stride-dimension byte
@@ -177,6 +179,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Transaction bytes a phase of the barrier will receive, without an arrival
+// (the arrival comes after the copy warp's own stores into the same stage).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 // 2-D TMA tile load (x = head dim, y = cache row) completing bytes on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
@@ -184,6 +192,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
           dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
 // Row reduction of 16 per-thread values (one per query row) over the 32 lanes
@@ -214,85 +226,84 @@ struct AddOp {
   __device__ float operator()(float x, float y) const { return x + y; }
 };
 
-// Chunk stream order shared by the producer and the MMA warp: K(0), V(0),
-// K(1), V(1), ... (tensor 0 = K, 1 = V). V(i) streams in while the softmax
-// warps work on S(i), so its P.V can start as soon as P(i) is written.
-__device__ __forceinline__ void stream_step(int step, int& tensor, int& tile) {
-  tensor = step & 1;
-  tile = step >> 1;
-}
-
-__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
-}
-
 struct UmmaMaps {
-  CUtensorMap k, v;            // boxes of 64 dims x 128 rows
-  CUtensorMap k_tail, v_tail;  // boxes of 64 dims x 8 rows
+  CUtensorMap k[um::NMAP], v[um::NMAP];  // boxes of 64 dims x 128, 64, 32, 16, 8 rows
 };
 
-template <int T_>
 __global__ void __launch_bounds__(um::THREADS, 1)
     split_umma_kernel(const __grid_constant__ UmmaMaps maps, const LaunchArgs a) {
   using namespace um;
-  using U = UmmaTile<T_>;
-  constexpr int T = U::T, CHUNK_BYTES = U::CHUNK_BYTES, NRING = U::NRING, OFF_RING = U::OFF_RING;
-  constexpr int OFF_Q = U::OFF_Q, OFF_P = U::OFF_P, P_HALF = U::P_HALF, P_BUF = U::P_BUF, OFF_RED = U::OFF_RED;
-  constexpr int OFF_BAR = U::OFF_BAR, OFF_TMEM = U::OFF_TMEM, LPQ = U::LPQ;
-  constexpr uint32_t kIdescQK = U::kIdescQK;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (base - raw);
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int S = a.num_splits;
   const int G = a.NH / a.NKV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hbase = kvh * G;
 
   const uint32_t bar0 = base + OFF_BAR;
-  const uint32_t full0 = bar0, empty0 = bar0 + 8 * NRING;
-  const uint32_t q_ready = bar0 + 16 * NRING;
-  const uint32_t s_full0 = q_ready + 8, p_ready0 = s_full0 + 16, pv_done = p_ready0 + 16;
+  const uint32_t full_k = bar0, empty_k = full_k + 8 * NK;
+  const uint32_t full_v = empty_k + 8 * NK, empty_v = full_v + 8 * NVP;
+  const uint32_t s_full = empty_v + 8 * NVP, s_free = s_full + 16, p_ready = s_free + 16, pv_done = p_ready + 16;
+  const uint32_t q_ready = pv_done + 16, mma_done = q_ready + 8;
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
 
-  // Set-up that reads no input, overlapping the previous kernel's tail. The
-  // ring starts zeroed: rows past a partial tile then hold zeros or earlier,
-  // finite cache rows, and their softmax weight is 0.
+  // Set-up that reads no input, overlapping the previous kernel's tail.
   if (tid == 0) {
-    for (int k = 0; k < NRING; ++k) {
-      mbar_init(full0 + 8 * k, 1);   // the producer's expect_tx arrival + the bytes
-      mbar_init(empty0 + 8 * k, 1);  // one tcgen05.commit
+    for (int k = 0; k < NK; ++k) {
+      mbar_init(full_k + 8 * k, 1);   // the copy warp's arrival + the bytes
+      mbar_init(empty_k + 8 * k, 1);  // one tcgen05.commit
+    }
+    for (int k = 0; k < NVP; ++k) {
+      mbar_init(full_v + 8 * k, 1);
+      mbar_init(empty_v + 8 * k, 1);
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(s_full + 8 * j, 1);
+      mbar_init(s_free + 8 * j, NSOFT * 32);
+      mbar_init(p_ready + 8 * j, NSOFT * 32);
+      mbar_init(pv_done + 8 * j, 1);
     }
     mbar_init(q_ready, NSOFT * 32);
-    for (int j = 0; j < 2; ++j) {
-      mbar_init(s_full0 + 8 * j, 1);
-      mbar_init(p_ready0 + 8 * j, NSOFT * 32);
-    }
-    mbar_init(pv_done, 1);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
-  if (tid == 32) {
-    prefetch_tensor_map(&maps.k);
-    prefetch_tensor_map(&maps.v);
-    prefetch_tensor_map(&maps.k_tail);
-    prefetch_tensor_map(&maps.v_tail);
+  if ((warp == W_K || warp == W_V) && lane == 0) {
+    const bool is_k = warp == W_K;
+#pragma unroll
+    for (int i = 0; i < NMAP; ++i) prefetch_tensor_map(is_k ? &maps.k[i] : &maps.v[i]);
+    // This split's first tile of the slots [0, min(min_len, capacity)),
+    // which every allowed length makes live: ask L2 for it while the previous
+    // kernel runs (a hint only; the copies come after the dependency wait).
+    const int band_min = min(max(a.min_len, 0), a.capacity);
+    if (band_min > 0) {
+      const int cmin = chunk_of(band_min, S, a.granule);
+      const long long p0 = static_cast<long long>(s) * cmin;
+      if (p0 < band_min) {
+        const int nmin =
+            static_cast<int>(min(static_cast<long long>(T), min(static_cast<long long>(cmin), band_min - p0)));
+        const size_t row = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity + static_cast<size_t>(p0);
+        prefetch_l2((is_k ? a.k : a.v) + row * HS, static_cast<uint32_t>(nmin) * HS * 2);
+      }
+    }
   }
-  for (int i = tid * 16; i < NRING * CHUNK_BYTES; i += THREADS * 16)
-    *reinterpret_cast<uint4*>(smem + OFF_RING + i) = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
-  __syncthreads();  // barriers initialised and the ring zeroed before any copy
+  __syncthreads();
   grid_dependency_wait();
   grid_launch_dependents();
 
   // This split's slots [q0, q0 + n) of the band's slot range [0, band).
+  const int len_b = a.lens[b];
+  const bool reporter = s == 0 && kvh == 0 && tid == 0;
+  if (reporter && len_b < a.min_len) atomicOr(&g_device_error, FD_DEVERR_MIN_LEN);
   int lo;
-  const int band = band_of(a.lens[b], a.capacity, a.window, s == 0 && kvh == 0 && tid == 0, &lo);
-  const int chunk = chunk_of(band, a.num_splits, a.granule);
+  const int band = band_of(len_b, a.capacity, a.window, reporter, &lo);
+  const int chunk = chunk_of(band, S, a.granule);
   const long long q0 = static_cast<long long>(s) * chunk;
-  const long long q1 = min(static_cast<long long>(band), q0 + chunk);
-  const int n = q0 < q1 ? static_cast<int>(q1 - q0) : 0;
-  const bool direct = a.num_splits == 1;
-  if (n == 0) {  // an empty slice (no TMEM was taken)
+  const int n = q0 < band ? static_cast<int>(min(static_cast<long long>(chunk), band - q0)) : 0;
+  const bool direct = S == 1;
+  if (n == 0) {  // an empty slice: no copy issued, no tensor memory taken
     if (direct) {  // len == 0 with one split: the output row is zero
       for (int i = tid; i < G * HS; i += THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / HS) * HS + i % HS;
@@ -305,126 +316,201 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     return;
   }
   const int ntiles = (n + T - 1) / T;
+  const int row0 = static_cast<int>((static_cast<long long>(b) * a.NKV + kvh) * a.capacity + q0);
   bool failed = false;
-  uint32_t tmem = 0;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      const int row0 = static_cast<int>((static_cast<long long>(b) * a.NKV + kvh) * a.capacity + q0);
-      int seq = 0;
-      for (int step = 0; step < 2 * ntiles; ++step) {
-        int tensor, tile;
-        stream_step(step, tensor, tile);
-        const int nv = min(T, n - tile * T);
-        const int y = row0 + tile * T;
-        const CUtensorMap* map = tensor ? (nv == T ? &maps.v : &maps.v_tail) : (nv == T ? &maps.k : &maps.k_tail);
-        const int boxes = nv == T ? 1 : (nv + TAIL_ROWS - 1) / TAIL_ROWS;
-        const uint32_t box_bytes = nv == T ? CHUNK_BYTES : TAIL_ROWS * 128;
-        for (int c = 0; c < NCH; ++c, ++seq) {
-          const int slot = seq % NRING, use = seq / NRING;
-          if (use > 0) mbar_wait(empty0 + 8 * slot, (use - 1) & 1, failed);
-          const uint32_t dst = base + OFF_RING + slot * CHUNK_BYTES;
-          const uint32_t fb = full0 + 8 * slot;
-          mbar_arrive_expect_tx(fb, boxes * box_bytes);
-          for (int r = 0; r < boxes; ++r) tma_load_2d(dst + r * box_bytes, map, c * DC, y + r * TAIL_ROWS, fb);
+  // The MMA warp allocates the tensor memory; it and the softmax warps meet
+  // before using it. The copy warps need none and start at once.
+  uint32_t tmem = 0;
+  if (warp >= W_MMA) {
+    if (warp == W_MMA) {
+      tmem_alloc(base + OFF_TMEM, TMEM_COLS);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    named_bar_sync(2, (1 + NSOFT) * 32);
+    tc_fence_after();
+    tmem = *reinterpret_cast<const uint32_t*>(smem + OFF_TMEM);
+  }
+
+  if (warp == W_K || warp == W_V) {
+    // ---------------------------------------------------------- copy warps
+    const bool is_k = warp == W_K;
+    const CUtensorMap* mp = is_k ? maps.k : maps.v;
+    const uint16_t* src = is_k ? a.k : a.v;
+    const int nring = is_k ? NK : NVP;
+    const int per = is_k ? 1 : 2;  // chunks per ring slot
+    const uint32_t ring = base + (is_k ? OFF_K : OFF_V);
+    const uint32_t slot_bytes = per * CHUNK_BYTES;
+    const uint32_t fullb = is_k ? full_k : full_v, emptyb = is_k ? empty_k : empty_v;
+    uint32_t st_issued = 0, st_par = 0;
+    int seq = 0;
+    for (int t = 0; t < ntiles; ++t) {
+      const int nv = min(T, n - t * T);
+      const int nv8 = nv & ~7;      // rows the TMA boxes bring
+      const int nrem = nv - nv8;    // the slice's last rows: loaded by the lanes
+      const int y0 = row0 + t * T;  // cache row of the tile's first position
+      // the tail rows of every chunk of this tile, all loads in flight at once
+      uint4 tailv[MAX_TAIL];
+      if (nrem > 0) {
+#pragma unroll
+        for (int k = 0; k < MAX_TAIL; ++k) {
+          const int i = lane + 32 * k;  // piece i: chunk i / (8 nrem), row nv8 + (i / 8) % nrem, piece i % 8
+          tailv[k] = make_uint4(0, 0, 0, 0);
+          if (i < NCH * nrem * 8) {
+            const int c = i / (nrem * 8), rr = nv8 + (i / 8) % nrem, j = i % 8;
+            tailv[k] = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(y0 + rr) * HS + c * DC + j * 8);
+          }
         }
       }
+      for (int u = 0; u < NCH / per; ++u, ++seq) {
+        const int slot = seq % nring, use = seq / nring;
+        if (use > 0) mbar_wait(emptyb + 8 * slot, (use - 1) & 1, failed);
+        const uint32_t dst = ring + slot * slot_bytes;
+        const uint32_t fb = fullb + 8 * slot;
+        unsigned char* dsts = smem + (dst - base);
+        if (!is_k && nv < T) {
+          // V rows past the tile's valid positions: zero, so their 0 weights
+          // add exactly 0 (stale shared memory may hold any bit pattern)
+          const int words = (T - nv) * (DC * 2 / 16);  // 16-byte words per chunk
+          for (int w = lane; w < 2 * words; w += 32) {
+            const int ch = w / words, rem = w % words;
+            *reinterpret_cast<uint4*>(dsts + ch * CHUNK_BYTES + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (lane == 0) {
+          mbar_expect_tx(fb, static_cast<uint32_t>(per * nv8) * 128);
+          for (int h = 0; h < per; ++h) {
+            const int c = u * per + h;
+            const uint32_t d = dst + h * CHUNK_BYTES;
+            if (nv8 == T) {
+              tma_load_2d(d, &mp[0], c * DC, y0, fb);
+            } else {
+              int r = 0;
+#pragma unroll
+              for (int bi = 1; bi < NMAP; ++bi) {
+                const int bh = T >> bi;
+                if (nv8 & bh) {
+                  tma_load_2d(d + r * 128, &mp[bi], c * DC, y0 + r, fb);
+                  r += bh;
+                }
+              }
+            }
+          }
+        }
+        if (nrem > 0) {
+          // rows [nv8, nv) of this slot's chunks: 16-byte pieces into the
+          // 128-byte swizzle (piece j of row r sits at 16 * (j ^ (r % 8)))
+#pragma unroll
+          for (int k = 0; k < MAX_TAIL; ++k) {
+            const int i = lane + 32 * k;
+            const int c = i / (nrem * 8);
+            if (i < NCH * nrem * 8 && c >= u * per && c < u * per + per) {
+              const int rr = nv8 + (i / 8) % nrem, j = i % 8;
+              *reinterpret_cast<uint4*>(dsts + (c - u * per) * CHUNK_BYTES + rr * 128 + ((j ^ (rr & 7)) << 4)) =
+                  tailv[k];
+            }
+          }
+        }
+        if (nrem > 0 || (!is_k && nv < T)) fence_proxy_async_smem();  // lanes' stores -> the tensor cores' view
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
+        st_issued |= 1u << slot;
+        st_par = (st_par & ~(1u << slot)) | (static_cast<uint32_t>(use & 1) << slot);
+      }
     }
-  } else {
-  // The producer needs no tensor memory and starts at once; warps 1-5 wait
-  // for warp 1's allocation.
-  if (warp == 1) {
-    tmem_alloc(base + OFF_TMEM, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  named_bar_sync(3, THREADS - 32);
-  tc_fence_after();
-  tmem = *reinterpret_cast<const uint32_t*>(smem + OFF_TMEM);
-
-  if (warp == 1) {
-    // ------------------------------------------------------- MMA issue warp
-    mbar_wait(q_ready, 0, failed);
-    tc_fence_after();
-    int seq = 0;
-    for (int step = 0; step < 2 * ntiles; ++step) {
-      int tensor, tile;
-      stream_step(step, tensor, tile);
-      if (tensor == 0) {
-        // S^T(tile) = K Q^T into S buffer tile % 2 (free: the softmax read
-        // S(tile - 2) before P(tile - 2) was ready, which P.V(tile - 2) and so
-        // this MMA waited for)
-        const uint32_t d = tmem + 16 * (tile & 1);
-        for (int c = 0; c < NCH; ++c, ++seq) {
-          const int slot = seq % NRING;
-          mbar_wait(full0 + 8 * slot, (seq / NRING) & 1, failed);
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t kb = base + OFF_RING + slot * CHUNK_BYTES;
-            const uint32_t qb = base + OFF_Q + c * ATOM_Q;
+    // No copy of this block may still be in flight when it leaves: wait for
+    // the last phase issued into each slot (bounded, own failure flag).
+    bool dfail = false;
+    for (int k = 0; k < nring; ++k)
+      if ((st_issued >> k) & 1u) mbar_wait(fullb + 8 * k, (st_par >> k) & 1u, dfail);
+  } else if (warp == W_MMA) {
+    // ----------------------------------------------------- MMA issue thread
+    if (lane == 0) {
+      mbar_wait(q_ready, 0, failed);
+      tc_fence_after();
+      int kt = 0, kc = 0, kseq = 0;  // next score MMAs: tile kt, chunk kc; K ring sequence
+      int vt = 0, vp = 0, vseq = 0;  // next P.V MMAs: tile vt, dims block vp; V ring sequence
+      bool s_ok = false, p_ok = false;
+      uint64_t t_idle = 0;
+      uint32_t spins = 0;  // polls without progress; the clock is read every 4096
+      while ((kt < ntiles || vt < ntiles) && !failed) {
+        bool prog = false;
+        if (kt < ntiles) {
+          // S buffer kt % 2 is free once the softmax has read S(kt - 2)
+          if (!s_ok) s_ok = kt < 2 || mbar_test(s_free + 8 * (kt & 1), ((kt - 2) >> 1) & 1);
+          const int slot = kseq % NK;
+          if (s_ok && mbar_test(full_k + 8 * slot, (kseq / NK) & 1)) {
+            tc_fence_after();
+            const uint32_t kb = base + OFF_K + slot * CHUNK_BYTES;
+            const uint32_t qb = base + OFF_Q + kc * ATOM_Q;
 #pragma unroll
             for (int kk = 0; kk < DC / 16; ++kk)
-              umma_bf16(d, sw128_desc(kb + 32 * kk, 16, 1024), sw128_desc(qb + 32 * kk, 16, 1024), kIdescQK,
-                        (c | kk) != 0);
-            umma_commit(empty0 + 8 * slot);
-          }
-          __syncwarp();
-        }
-        if (lane == 0) umma_commit(s_full0 + 8 * (tile & 1));
-        __syncwarp();
-      } else {
-        // O^T += V^T P^T(tile), 128 dims (two chunks) per MMA block
-        mbar_wait(p_ready0 + 8 * (tile & 1), (tile >> 1) & 1, failed);
-        tc_fence_after();
-        const int nv = min(T, n - tile * T);
-        const uint32_t pb = base + OFF_P + (tile & 1) * P_BUF;
-        for (int mb = 0; mb < NCH / 2; ++mb, seq += 2) {
-          const int slot = seq % NRING;  // even: slot + 1 is the pair's second chunk
-          mbar_wait(full0 + 8 * slot, (seq / NRING) & 1, failed);
-          mbar_wait(full0 + 8 * (slot + 1), ((seq + 1) / NRING) & 1, failed);
-          if (nv < T) {
-            // rows [nv, nv rounded up to 8) came from slots past the split:
-            // zero them (their weight is 0, but they may hold NaN)
-            const int r1 = min(T, (nv + TAIL_ROWS - 1) / TAIL_ROWS * TAIL_ROWS);
-            const int words = (r1 - nv) * 8;  // 16-byte words per chunk
-            for (int w = lane; w < 2 * words; w += 32) {
-              const int ch = w / words, rem = w % words;
-              *reinterpret_cast<uint4*>(smem + OFF_RING + (slot + ch) * CHUNK_BYTES + (nv + rem / 8) * 128 +
-                                        (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+              umma_bf16(tmem + 16 * (kt & 1), sw128_desc(kb + 32 * kk, 16, 1024), sw128_desc(qb + 32 * kk, 16, 1024),
+                        kIdescQK, (kc | kk) != 0);
+            umma_commit(empty_k + 8 * slot);
+            ++kseq;
+            if (++kc == NCH) {
+              umma_commit(s_full + 8 * (kt & 1));
+              kc = 0;
+              ++kt;
+              s_ok = false;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
+            prog = true;
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t d = tmem + 32 + 16 * mb;
-            const uint32_t vb = base + OFF_RING + slot * CHUNK_BYTES;
+        }
+        if (vt < kt) {
+          if (!p_ok) p_ok = mbar_test(p_ready + 8 * (vt & 1), (vt >> 1) & 1);
+          const int slot = vseq % NVP;
+          if (p_ok && mbar_test(full_v + 8 * slot, (vseq / NVP) & 1)) {
+            tc_fence_after();
+            const uint32_t vb = base + OFF_V + slot * PAIR_BYTES;
+            const uint32_t pb = base + OFF_P + (vt & 1) * P_BUF;
+            const uint32_t d = tmem + 32 + 16 * vp;
 #pragma unroll
             for (int kk = 0; kk < T / 16; ++kk) {
               const uint64_t adesc = sw128_desc(vb + kk * 2048, CHUNK_BYTES, 1024);
               const uint32_t patom = pb + (kk >> 2) * ATOM_Q + (kk & 3) * 32;
-              umma_bf16(d, adesc, sw128_desc(patom, 16, 1024), kIdescPV, (tile > 0 || kk > 0) ? 1u : 0u);
+              umma_bf16(d, adesc, sw128_desc(patom, 16, 1024), kIdescPV, (vt > 0 || kk > 0) ? 1u : 0u);
               umma_bf16(d, adesc, sw128_desc(patom + P_HALF, 16, 1024), kIdescPV, 1u);
             }
-            umma_commit(empty0 + 8 * slot);
-            umma_commit(empty0 + 8 * (slot + 1));
+            umma_commit(empty_v + 8 * slot);
+            ++vseq;
+            if (++vp == NCH / 2) {
+              umma_commit(pv_done + 8 * (vt & 1));
+              vp = 0;
+              ++vt;
+              p_ok = false;
+            }
+            prog = true;
           }
-          __syncwarp();
         }
-        if (lane == 0) umma_commit(pv_done);
-        __syncwarp();
+        if (prog) {
+          spins = 0;
+        } else if ((++spins & 4095u) == 0) {
+          const uint64_t now = globaltimer_ns();
+          if (spins == 4096u) {
+            t_idle = now;
+          } else if (now - t_idle > g_wait_limit_ns) {
+            failed = true;
+            atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);
+          }
+        }
       }
+      // every MMA issued has completed before the block can release the
+      // tensor memory
+      umma_commit(mma_done);
+      bool dfail = false;
+      mbar_wait(mma_done, 0, dfail);
     }
+    __syncwarp();
   } else {
-    // ------------------------------------------------- softmax / epilogue warps
-    const int sw = warp - 2;             // 0..3
-    const int quarter = warp & 3;        // the TMEM lane quarter this warp may access
-    const int tq = tid - 64;             // 0..127
-    // tile position whose S row this thread's TMEM lane holds (lanes >= LPQ of
-    // a quarter hold none when T = 64)
-    const bool lane_ok = lane < LPQ;
-    const int pl = quarter * LPQ + (lane & (LPQ - 1));
+    // ---------------------------------------------- softmax / epilogue warps
+    const int sw = warp - W_SOFT0;  // 0..3
+    const int quarter = warp & 3;   // the TMEM lane quarter this warp may access
+    const int tq = tid - W_SOFT0 * 32;
+    const int pl = quarter * 32 + lane;  // tile position whose S row this thread's TMEM lane holds
     const uint32_t tlane = static_cast<uint32_t>(quarter * 32) << 16;
 
     // Q -> shared memory as the K-major, 128-byte-swizzled B operand: atom c
@@ -448,70 +534,47 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     fence_proxy_async_smem();
     mbar_arrive(q_ready);
 
-    float m_run[NQ], l_run[NQ];
+    float m_use[NQ], l_part[NQ];  // reference maxima (log2 units); this thread's share of the row sums
 #pragma unroll
     for (int r = 0; r < NQ; ++r) {
-      m_run[r] = kNegInf;
-      l_run[r] = 0.f;
+      m_use[r] = kNegInf;
+      l_part[r] = 0.f;
     }
     for (int i = 0; i < ntiles; ++i) {
       const int nv = min(T, n - i * T);
-      mbar_wait(s_full0 + 8 * (i & 1), (i >> 1) & 1, failed);
+      mbar_wait(s_full + 8 * (i & 1), (i >> 1) & 1, failed);
       tc_fence_after();
       float sc[NQ];
       tmem_ld16(tmem + tlane + 16 * (i & 1), sc);
-      const bool valid = lane_ok && pl < nv;
+      tc_fence_before();
+      mbar_arrive(s_free + 8 * (i & 1));  // S(i) read: its buffer may take S(i + 2)
+      const bool valid = pl < nv;
 #pragma unroll
       for (int r = 0; r < NQ; ++r) sc[r] = valid ? sc[r] * a.scale_log2 : kNegInf;
 
-      // row maxima of the tile: warp butterfly, then the four warps' values
+      // the tile's row maxima: warp butterfly, then the four warps' values
+      float* rm = red + (i & 1) * NQ * NSOFT;
       const float wmax = rowreduce16(sc, lane, MaxOp());
-      if ((lane & 1) == 0) red[(lane >> 1) * NSOFT + sw] = wmax;
-      named_bar_sync(2, NSOFT * 32);
-      float m_new[NQ], alpha[NQ], p[NQ];
+      if ((lane & 1) == 0) rm[(lane >> 1) * NSOFT + sw] = wmax;
+      named_bar_sync(1, NSOFT * 32);
+      bool resc = false;
+      float alpha[NQ];
 #pragma unroll
       for (int r = 0; r < NQ; ++r) {
-        const float4 t = *reinterpret_cast<const float4*>(red + r * NSOFT);
-        m_new[r] = fmaxf(m_run[r], fmaxf(fmaxf(t.x, t.y), fmaxf(t.z, t.w)));
-        alpha[r] = m_new[r] == kNegInf ? 1.f : exp2f(m_run[r] - m_new[r]);
-        p[r] = m_new[r] == kNegInf ? 0.f : exp2f(sc[r] - m_new[r]);
+        const float4 t4 = *reinterpret_cast<const float4*>(rm + r * NSOFT);
+        const float mt = fmaxf(fmaxf(t4.x, t4.y), fmaxf(t4.z, t4.w));
+        const bool need = mt > m_use[r] + kRescaleLog2;  // false for -inf and NaN tile maxima
+        alpha[r] = need ? exp2f(m_use[r] - mt) : 1.f;
+        if (need) m_use[r] = mt;
+        resc |= need;
       }
-
-      // P = hi + lo bf16 -> buffer i % 2, K-major and swizzled like Q (its
-      // last reader, P.V(i - 2), finished before tile i - 1 released its P)
-      {
-        unsigned char* pbuf = smem + OFF_P + (i & 1) * P_BUF + (pl >> 6) * ATOM_Q;
-        const int pc = (pl & 63) >> 3, pw = (pl & 7) * 2;
-        if (lane_ok) {
+      // every thread took the same decision from the same shared values
+      if (resc) {
 #pragma unroll
-          for (int r = 0; r < NQ; ++r) {
-            const uint16_t hi = f32_to_bf16_bits(p[r]);
-            const uint16_t lo = f32_to_bf16_bits(p[r] - bf16_bits_to_f32(hi));
-            unsigned char* at = pbuf + (r >> 3) * 1024 + (r & 7) * 128 + ((pc ^ (r & 7)) << 4) + pw;
-            *reinterpret_cast<uint16_t*>(at) = hi;
-            *reinterpret_cast<uint16_t*>(at + P_HALF) = lo;
-          }
-        }
-      }
-
-      // row sums
-      const float wsum = rowreduce16(p, lane, AddOp());
-      if ((lane & 1) == 0) red[NQ * NSOFT + (lane >> 1) * NSOFT + sw] = wsum;
-      named_bar_sync(2, NSOFT * 32);
-      bool moved = false;
-#pragma unroll
-      for (int r = 0; r < NQ; ++r) {
-        const float4 t = *reinterpret_cast<const float4*>(red + NQ * NSOFT + r * NSOFT);
-        l_run[r] = l_run[r] * alpha[r] + ((t.x + t.y) + (t.z + t.w));
-        moved |= alpha[r] != 1.f;
-      }
-
-      // O *= alpha in tensor memory once P.V(i - 1) is done (every thread
-      // holds the same alphas, so the branch is uniform)
-      if (i > 0) {
-        mbar_wait(pv_done, (i - 1) & 1, failed);
-        tc_fence_after();
-        if (moved) {
+        for (int r = 0; r < NQ; ++r) l_part[r] *= alpha[r];
+        if (i > 0) {  // O holds P.V of the earlier tiles: rescale it once P.V(i - 1) is done
+          mbar_wait(pv_done + 8 * ((i - 1) & 1), ((i - 1) >> 1) & 1, failed);
+          tc_fence_after();
 #pragma unroll
           for (int mb = 0; mb < NCH / 2; ++mb) {
             float o[NQ];
@@ -523,15 +586,45 @@ __global__ void __launch_bounds__(um::THREADS, 1)
           tmem_st_wait();
         }
       }
+      float p[NQ];
 #pragma unroll
-      for (int r = 0; r < NQ; ++r) m_run[r] = m_new[r];
+      for (int r = 0; r < NQ; ++r) {
+        p[r] = exp2f(sc[r] - m_use[r]);
+        l_part[r] += p[r];
+      }
+
+      // P = hi + lo bf16 -> buffer i % 2, K-major and swizzled like Q; its
+      // last reader, P.V(i - 2), must be done
+      if (i >= 2) mbar_wait(pv_done + 8 * (i & 1), ((i - 2) >> 1) & 1, failed);
+      {
+        unsigned char* pbuf = smem + OFF_P + (i & 1) * P_BUF + (pl >> 6) * ATOM_Q;
+        const int pc = (pl & 63) >> 3, pw = (pl & 7) * 2;
+#pragma unroll
+        for (int r = 0; r < NQ; ++r) {
+          const uint16_t hi = f32_to_bf16_bits(p[r]);
+          const uint16_t lo16 = f32_to_bf16_bits(p[r] - bf16_bits_to_f32(hi));
+          unsigned char* at = pbuf + (r >> 3) * 1024 + (r & 7) * 128 + ((pc ^ (r & 7)) << 4) + pw;
+          *reinterpret_cast<uint16_t*>(at) = hi;
+          *reinterpret_cast<uint16_t*>(at + P_HALF) = lo16;
+        }
+      }
       fence_proxy_async_smem();  // P stores -> the tensor cores' view of shared memory
       tc_fence_before();
-      mbar_arrive(p_ready0 + 8 * (i & 1));
+      mbar_arrive(p_ready + 8 * (i & 1));
     }
 
-    // ---- epilogue: this thread's dim of each 128-dim block, all rows
-    mbar_wait(pv_done, (ntiles - 1) & 1, failed);
+    // ---- epilogue: the row sums, then this thread's dim of each 128-dim block
+    float* rs = red + 2 * NQ * NSOFT;
+    const float lsum = rowreduce16(l_part, lane, AddOp());
+    if ((lane & 1) == 0) rs[(lane >> 1) * NSOFT + sw] = lsum;
+    named_bar_sync(1, NSOFT * 32);
+    float L[NQ];
+#pragma unroll
+    for (int r = 0; r < NQ; ++r) {
+      const float4 t4 = *reinterpret_cast<const float4*>(rs + r * NSOFT);
+      L[r] = (t4.x + t4.y) + (t4.z + t4.w);  // fixed order
+    }
+    mbar_wait(pv_done + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1, failed);
     tc_fence_after();
 #pragma unroll
     for (int mb = 0; mb < NCH / 2; ++mb) {
@@ -543,33 +636,31 @@ __global__ void __launch_bounds__(um::THREADS, 1)
         if (r >= G) break;
         const size_t row = static_cast<size_t>(b) * a.NH + hbase + r;
         if (direct) {
-          const float x = o[r] / l_run[r];
+          const float x = o[r] / L[r];
           a.out[row * HS + d] = f32_to_bf16_bits(x);
           if (a.out_f32) a.out_f32[row * HS + d] = x;
         } else {
-          a.ws_o[(row * a.num_splits + s) * HS + d] = o[r];
+          a.ws_o[(row * S + s) * HS + d] = o[r];
         }
       }
     }
     if (!direct && tq < G) {
-      const size_t row = static_cast<size_t>(b) * a.NH + hbase + tq;
-      float mr = m_run[0], lr = l_run[0];
+      float mr = m_use[0], lr = L[0];
 #pragma unroll
       for (int r = 1; r < NQ; ++r)
         if (r == tq) {
-          mr = m_run[r];
-          lr = l_run[r];
+          mr = m_use[r];
+          lr = L[r];
         }
-      a.ws_ml[(row * a.num_splits + s) * 2 + 0] = mr;
-      a.ws_ml[(row * a.num_splits + s) * 2 + 1] = lr;
+      const size_t row = static_cast<size_t>(b) * a.NH + hbase + tq;
+      reinterpret_cast<float2*>(a.ws_ml)[row * S + s] = make_float2(mr, lr);
     }
-  }
   }
 
   // release the tensor memory once every warp is done with it
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -588,48 +679,86 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// The cache [B * NKV * capacity rows][512 dims] as a 2-D bf16 tensor with
-// 128-byte swizzled boxes of 64 dims x `rows`.
-bool encode_cache_map(CUtensorMap* m, const void* base, const LaunchArgs& a, uint32_t rows) {
+// A cache [rows][512 dims] as a 2-D bf16 tensor with 128-byte swizzled boxes
+// of 64 dims x `box_rows`.
+bool encode_cache_map(CUtensorMap* m, const void* base, long long rows, uint32_t box_rows) {
   const auto enc = tensor_map_encoder();
   if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(um::HS),
-                              static_cast<cuuint64_t>(a.B) * a.NKV * static_cast<cuuint64_t>(a.capacity)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(um::HS), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(um::HS) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(um::DC), rows};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(um::DC), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Encoded maps of recent (K, V, rows) caches: encoding ten maps costs several
+// microseconds of host time, and a decode loop calls with the same caches
+// every step. Direct-mapped by the K address.
+struct MapEntry {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  long long rows = 0;
+  UmmaMaps maps;
+};
+constexpr int kMapCache = 128;
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCache];
+
+bool cached_maps(const LaunchArgs& a, UmmaMaps* out) {
+  const long long rows = static_cast<long long>(a.B) * a.NKV * a.capacity;
+  const size_t slot = (reinterpret_cast<uintptr_t>(a.k) >> 12) % kMapCache;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry& e = g_map_cache[slot];
+  if (e.k != a.k || e.v != a.v || e.rows != rows) {
+    UmmaMaps m;
+    for (int i = 0; i < um::NMAP; ++i) {
+      const uint32_t h = static_cast<uint32_t>(um::T >> i);
+      if (!encode_cache_map(&m.k[i], a.k, rows, h) || !encode_cache_map(&m.v[i], a.v, rows, h)) return false;
+    }
+    e.k = a.k;
+    e.v = a.v;
+    e.rows = rows;
+    e.maps = m;
+  }
+  *out = e.maps;
+  return true;
+}
+
 }  // namespace
 
 bool umma_shape_ok(int HS, int G, int window) { return HS == um::HS && G > 8 && G <= um::NQ && window <= 0; }
+
+int umma_tile_positions() { return um::T; }
 
 cudaError_t launch_umma(const LaunchArgs& a, cudaStream_t stream) {
   if (!umma_shape_ok(a.HS, a.NH / a.NKV, a.window) || a.cluster != 1 || a.fused || a.kv8 ||
       static_cast<long long>(a.B) * a.NKV * a.capacity >= (1ll << 31))
     return cudaErrorInvalidValue;
   UmmaMaps maps;
-  if (!encode_cache_map(&maps.k, a.k, a, kUmmaTile) || !encode_cache_map(&maps.v, a.v, a, kUmmaTile) ||
-      !encode_cache_map(&maps.k_tail, a.k, a, um::TAIL_ROWS) || !encode_cache_map(&maps.v_tail, a.v, a, um::TAIL_ROWS))
-    return cudaErrorInvalidValue;
-  constexpr int kSmem = UmmaTile<kUmmaTile>::SMEM;
-  cudaError_t e =
-      cudaFuncSetAttribute(split_umma_kernel<kUmmaTile>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (!cached_maps(a, &maps)) return cudaErrorInvalidValue;
+  static std::atomic<unsigned long long> attr_done{0};  // bit d: attribute set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit == 0 || (attr_done.load(std::memory_order_acquire) & bit) == 0) {
+    e = cudaFuncSetAttribute(split_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, um::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_acq_rel);
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.num_splits, a.NKV, a.B);
   cfg.blockDim = dim3(um::THREADS);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = um::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_umma_kernel<kUmmaTile>, maps, a);
+  return cudaLaunchKernelEx(&cfg, split_umma_kernel, maps, a);
 }
 
 cudaError_t set_wait_limit_umma(unsigned long long ns) {

@@ -139,13 +139,17 @@ enum {
  *
  * Tensor-memory kernel (opt-in through fd_plan_override(..., FD_PATH_UMMA, ...);
  * plans never choose it): for the MQA geometry of "One KV head breaks the
- * textbook" (bf16, HS 512, 8 < G <= 16, window <= 0) the split blocks stream
- * K and V as 128-position TMA tiles and run S^T = K Q^T and O^T += V^T P^T as
- * tcgen05 MMAs with the accumulators in tensor memory; with no window the
- * band's slots are [0, min(len, capacity)), walked in slot order. Such a plan
+ * textbook" (bf16, HS 512, 8 < G <= 16, window <= 0) each split block takes a
+ * consecutive slice of the band's slots [0, min(len, capacity)), streams K and
+ * V through two separate shared-memory rings as TMA boxes of 128/64/32/16/8
+ * rows (the last rows of a slice that do not fill 8 are loaded by the copy
+ * warp, so exactly the band is read), and one thread issues S^T = K Q^T and
+ * O^T += V^T P^T as tcgen05 MMAs with the accumulators in tensor memory,
+ * the next tile's scores while the current tile's softmax runs. Such a plan
  * has group_bytes = 16384 (one TMA box), consumer_warps = 4, cluster = 1 and
  * no fused merge; the merge kernel is the same. Measured slower than
- * FD_PATH_TC on GB300 (the 256 KB tile outgrows the shared-memory ring).
+ * FD_PATH_TC on GB300 (a 128-position tile of K and V is larger than shared
+ * memory, so each block streams at about 60% of its share of HBM).
  *
  * Clusters (opt-in through fd_plan_override; plans use cluster = 1): the
  * blocks of `cluster` consecutive splits form a thread-block cluster and

@@ -139,3 +139,26 @@ def test_umma_full_size_workload_sampled_rows(name):
     del q, k, v
     torch.cuda.empty_cache()
     check(res, oracle_ref(w, qh, kh, vh, lens, rows=rows), rows=rows, what=name)
+
+
+def test_umma_rising_scores_rescale_across_tiles():
+    """Scores that grow tile after tile by more than the 2^8 the running
+    maximum may lag behind: the rescale of O in tensor memory runs at several
+    tile boundaries, and at S = 1 one block sees them all."""
+    w = W("u_rising", 1, 16, 1, 512, 1024, 0, lens=(1000,), seed=75)
+    q, k, v, lens = make_inputs(w)
+    ramp = torch.linspace(0.2, 6.0, w.capacity).view(1, 1, -1, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    ref = oracle_ref(w, q, k, v, lens)
+    for s in (1, 3):
+        check(_umma_run(w, q, k, v, lens, splits=s), ref, what=f"rising S={s}")
+
+
+def test_umma_nan_key_in_a_middle_tile_reaches_every_row():
+    w = W("u_nan_k", 1, 16, 1, 512, 1024, 0, lens=(900,), seed=76)
+    q, k, v, lens = make_inputs(w)
+    k[0, 0, 400, 3] = float("nan")
+    res = _umma_run(w, q, k, v, lens, splits=1)
+    assert torch.isnan(res["out32"][0]).all()
+    res = _umma_run(w, q, k, v, lens, splits=4)
+    assert torch.isnan(res["out32"][0]).all()
