@@ -100,11 +100,11 @@ int persistent_rule(const fd_plan_t& p) {
 }
 
 // Fused merge (the last split block of each (sequence, KV head) merges) when
-// the group's partials are few and small: G * S weights fit the block's score
-// buffer and the partials stay within 256 KB per group.
+// the group's partials, which that one block reads, stay within 256 KB.
 bool fused_rule_allowed(const fd_plan_t& p) {
   const long long G = p.NH / p.NKV;
-  return p.path == FD_PATH_TC && p.cluster == 1 && slots(p) > 1 && G * p.num_splits <= 480;
+  return p.path == FD_PATH_TC && p.cluster == 1 && slots(p) > 1 &&
+         G * p.num_splits * p.HS * static_cast<long long>(sizeof(float)) <= (256ll << 10);
 }
 
 // Off by default: measured on GB300, the separate merge kernel (already

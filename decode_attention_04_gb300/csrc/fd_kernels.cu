@@ -225,7 +225,7 @@ size_t simt_smem_bytes(int G, int HS) {
 // MMA 2c holds dim 32c + 4 grp, row grp + 8 dim 32c + 4 grp + 1, and MMA
 // 2c + 1 the dims + 2 and + 3. With the 16-byte group padding both load
 // patterns are free of bank conflicts.
-template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048, bool KV8_ = false>
+template <int HS_, int NT_, int NWC_, int NSTAGE_, int GROUP_BYTES_ = 2048, bool KV8_ = false, int MAXREG_ = 0>
 struct TcCfg {
   static constexpr bool KV8 = KV8_;
   static constexpr int HS = HS_;
@@ -262,6 +262,24 @@ struct TcCfg {
   static constexpr size_t OFF_A = OFF_P + static_cast<size_t>(2) * NP * PPITCH * 2;  // f32 alpha,m,l [NP]
   static constexpr size_t OFF_BAR = (OFF_A + 3 * NP * 4 + 7) / 8 * 8;        // u64 full[], empty[]
   static constexpr size_t SMEM = OFF_BAR + 2 * NSTAGE * 8;
+  // blocks per SM the shared memory allows (two when a block takes at most
+  // half of the SM's 228 KB, less the 1 KB the driver reserves per block);
+  // the fused-merge instance is held to it by a register bound (the plain
+  // instance is left to the compiler, which keeps it leaner)
+  static constexpr int MINB = SMEM + 1024 <= 114 * 1024 ? 2 : 1;
+  // Register budget of the plain per-split instance (0: the compiler's
+  // choice, under launch bounds only), set where a measurement depends on it
+  // (GB300, us per layer): a tile meant to run two blocks per SM must fit
+  // twice (the bf16 MQA tile at 106 registers ran one block per SM, two
+  // waves: 212 against 164 for MQA long), and the one-block-per-SM MQA tiles
+  // ran best at 96 (E4M3 MQA 32k 22.5 at 119 registers, 21.7 at 96). A
+  // budget given to every instance slowed others (E4M3 MQA long 122 -> 144),
+  // so only these configurations take one. Where one-tile splits wait for the
+  // merge kernel, that kernel's blocks must fit beside two split blocks (the
+  // ring tile at 82 registers, where none fits, 7.0; the compiler's choice
+  // without the fused merge in the instance, 6.1). The fused-merge instance
+  // is held by its launch bounds to the occupancy its shared memory allows.
+  static constexpr int MAXREG = MAXREG_;
 
   // tile position held by MMA row m, and its byte offset in a stage
   __device__ static __forceinline__ int pos_of(int m) { return (m % NG) * R + m / NG; }
@@ -290,7 +308,6 @@ struct TcCfg {
                 "E4M3 groups are 1 or 2 KB, 16-byte aligned");
   static_assert(!KV8 || DW % 32 == 0, "E4M3 fragments take head dims 32 at a time");
   static_assert(NP * 16 + 2 * NP <= NWC * NP * SP, "cluster weights must fit the score buffer");
-  static_assert(NWC * NP * SP >= 480, "fused-merge weights (G * S <= 480) must fit the score buffer");
 };
 
 constexpr int kLptMaxB = 64;
@@ -365,6 +382,14 @@ __device__ __forceinline__ void produce_tile(const LaunchArgs& a, const unsigned
 // block is still in flight when the block exits. Earlier phases of a stage
 // completed before that stage was issued again, and only the producers
 // arrive on the full barriers, so the last issued phase is the last phase.
+// Atomic increment with wrap ((old >= limit) ? 0 : old + 1) and
+// acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned* p, unsigned limit) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+  return old;
+}
+
 template <class C>
 __device__ __forceinline__ void producer_drain(uint32_t full0, uint32_t st_issued, uint32_t st_par) {
   bool dfail = false;
@@ -373,8 +398,13 @@ __device__ __forceinline__ void producer_drain(uint32_t full0, uint32_t st_issue
     if ((st_issued >> st) & 1u) mbar_wait(full0 + 8 * st, (st_par >> st) & 1u, dfail);
 }
 
-template <class C, bool PERSIST = false>
-__global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a) {
+// The split kernel's body. PERSIST: the persistent grid; FUSED: the last block
+// of each group merges. Each is a separate instance, so the plain per-split
+// kernel keeps its registers (on GB300 every register it gains can keep the
+// merge kernel's blocks, which wait beside it under programmatic dependent
+// launch, off the SM).
+template <class C, bool PERSIST, bool FUSED>
+__device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_seq[kLptMaxB];
   __shared__ int s_item[kItemQ];
@@ -547,13 +577,13 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
     if (!persist && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
     // len == 0: the output row is zero. With one block per band, or with the
     // fused merge (no block of an empty band ever merges), block 0 writes it.
-    if (direct || (a.fused && band == 0 && s == 0)) {
+    if (direct || (FUSED && band == 0 && s == 0)) {
       for (int i = tid; i < G * C::HS; i += C::THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / C::HS) * C::HS + i % C::HS;
         a.out[o] = 0;
         if (a.out_f32) a.out_f32[o] = 0.f;
       }
-    } else if (!a.fused) {
+    } else if (!FUSED) {
       write_empty_partial(a, b, hbase, G, C::HS, s, tid, C::THREADS);
     }
     continue;
@@ -923,89 +953,90 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       a.ws_ml[r] = sM[tid];
       a.ws_ml[r + 1] = sL[tid];
     }
-    if (direct || !a.fused) continue;
+    if constexpr (!FUSED) continue;
+    if (direct) continue;
 
     // ---- fused merge: the last block of this (sequence, KV head) to finish
-    // combines every partial of the group (no merge launch). The counter
-    // wraps to zero as the last block takes it, so it is zero again for the
-    // next call.
+    // combines every partial of the group (no merge launch). Thread 0 counts
+    // the block in with one acquire-release atomic: its release publishes the
+    // block's partial stores (the barrier ordered them before it), its
+    // acquire makes every earlier block's partials visible here (the barrier
+    // after it passes that on to the block). The counter wraps to zero as the
+    // last block takes it, so it is zero again for the next call. The last
+    // block loads each (row, 4 dims) item's partials and their (m, l) in one
+    // round trip per batch and folds them online; when there are fewer items
+    // than threads, JG threads share an item's splits and meet in shared
+    // memory in a fixed order.
     __shared__ int s_last;
     const int nsplit = nact;
-    named_bar_sync(1, C::CTHREADS);  // every thread's partial stores precede ...
-    if (tid == 0) {
-      __threadfence();  // ... this fence (cumulative), so they are visible before the count
-      s_last = atomicInc(a.counters + static_cast<size_t>(b) * a.NKV + kvh, static_cast<unsigned>(nsplit - 1)) ==
+    named_bar_sync(1, C::CTHREADS);  // every thread's partial stores precede thread 0's release
+    if (tid == 0)
+      s_last = atom_inc_acq_rel(a.counters + static_cast<size_t>(b) * a.NKV + kvh, static_cast<unsigned>(nsplit - 1)) ==
                static_cast<unsigned>(nsplit - 1);
-      __threadfence();  // and every counted partial is visible after it
-    }
     named_bar_sync(1, C::CTHREADS);
     if (!s_last) return;
 
     const int S = a.num_splits;
-    float* sW = sS;            // [G][nsplit] weights 2^(m_s - M)
-    float* sLt = sAlpha;       // [G] sum of weighted l
-    for (int g = warp; g < G; g += C::NWC) {
-      const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + (static_cast<size_t>(b) * a.NH + hbase + g) * S;
-      float M = kNegInf;
-      for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, __ldcg(&ml[j].x));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      float L = 0.f;
-      for (int j = lane; j < nsplit; j += 32) {
-        const float2 v = __ldcg(&ml[j]);
-        const float w = exp2f(v.x - M);
-        sW[g * nsplit + j] = w;
-        L += w * v.y;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-      if (lane == 0) sLt[g] = L;
-    }
-    named_bar_sync(1, C::CTHREADS);
-    // O = sum_j w_j O_j / L per (row, 4 dims). When there are fewer such items
-    // than threads, each item's splits are divided among JG threads, so every
-    // thread has all its loads in flight at once; their sums meet in shared
-    // memory behind the weights.
     constexpr int D4 = C::HS / 4;
-    constexpr int kFusedBatch = 16;
+    constexpr int kFusedBatch = 8;
     const int items = G * D4;
     int JG = C::CTHREADS / items;
-    if (JG < 1 || 512 + 4 * C::CTHREADS > C::NWC * C::NP * C::SP) JG = 1;
-    float4* sAcc = reinterpret_cast<float4*>(sS + 512);  // [JG][items], after sW (G * nsplit <= 480)
+    if (JG < 1 || static_cast<size_t>(JG) * items * 24 > static_cast<size_t>(C::NWC) * C::NP * C::SP * 4) JG = 1;
+    float4* sAcc = reinterpret_cast<float4*>(sS);                 // [JG][items] weighted O sums
+    float2* sMl = reinterpret_cast<float2*>(sAcc + JG * items);  // [JG][items] (max, weighted l)
+    auto store_out = [&](size_t row, int d, float4 acc, float L) {
+      const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+      const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+      const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                           (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+      *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+    };
     for (int t = tid; t < items * JG; t += C::CTHREADS) {
       const int item = t % items, jg = t / items;
       const int g = item / D4, d = (item % D4) * 4;
       const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
       const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * S * C::HS + d);
+      const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row * S;
+      float M = kNegInf, L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j0 = jg; j0 < nsplit; j0 += kFusedBatch * JG) {
         float4 v[kFusedBatch];
+        float2 w2[kFusedBatch];
 #pragma unroll
-        for (int u = 0; u < kFusedBatch; ++u) {
+        for (int u = 0; u < kFusedBatch; ++u) {  // every load of the batch in flight at once
           const int j = j0 + u * JG;
           v[u] = j < nsplit ? __ldcg(src + static_cast<size_t>(j) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          w2[u] = j < nsplit ? __ldcg(ml + j) : make_float2(kNegInf, 0.f);
         }
+        float bm = kNegInf;
+#pragma unroll
+        for (int u = 0; u < kFusedBatch; ++u) bm = fmaxf(bm, w2[u].x);
+        const float mn = fmaxf(M, bm);
+        if (mn == kNegInf) continue;  // nothing but empty partials so far
+        const float sc = exp2f(M - mn);  // 0 while M is still -inf
+        L *= sc;
+        acc.x *= sc;
+        acc.y *= sc;
+        acc.z *= sc;
+        acc.w *= sc;
 #pragma unroll
         for (int u = 0; u < kFusedBatch; ++u) {
-          const int j = j0 + u * JG;
-          const float w = j < nsplit ? sW[g * nsplit + j] : 0.f;
+          const float w = exp2f(w2[u].x - mn);  // 0 for padding and empty partials
+          L += w * w2[u].y;
           acc.x += w * v[u].x;
           acc.y += w * v[u].y;
           acc.z += w * v[u].z;
           acc.w += w * v[u].w;
         }
+        M = mn;
       }
-      if (JG > 1) {
-        sAcc[jg * items + item] = acc;
+      if (JG == 1) {
+        store_out(row, d, acc, L);
       } else {
-        const float L = sLt[g];
-        const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
-        const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
-                             (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
-        const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
-                             (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
-        *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
-        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+        sAcc[jg * items + item] = acc;
+        sMl[jg * items + item] = make_float2(M, L);
       }
     }
     if (JG > 1) {
@@ -1013,22 +1044,21 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
       for (int item = tid; item < items; item += C::CTHREADS) {
         const int g = item / D4, d = (item % D4) * 4;
         const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
-        float4 acc = sAcc[item];
-        for (int jg = 1; jg < JG; ++jg) {  // fixed order: the result does not depend on timing
+        float M = kNegInf;
+        for (int jg = 0; jg < JG; ++jg) M = fmaxf(M, sMl[jg * items + item].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int jg = 0; jg < JG; ++jg) {  // fixed order: the result does not depend on timing
+          const float2 ml = sMl[jg * items + item];
+          const float w = ml.x == kNegInf ? 0.f : exp2f(ml.x - M);
           const float4 o2 = sAcc[jg * items + item];
-          acc.x += o2.x;
-          acc.y += o2.y;
-          acc.z += o2.z;
-          acc.w += o2.w;
+          L += w * ml.y;
+          acc.x += w * o2.x;
+          acc.y += w * o2.y;
+          acc.z += w * o2.z;
+          acc.w += w * o2.w;
         }
-        const float L = sLt[g];
-        const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
-        const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
-                             (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
-        const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
-                             (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
-        *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
-        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+        store_out(row, d, acc, L);
       }
     }
     return;
@@ -1113,6 +1143,18 @@ __global__ void __launch_bounds__(C::THREADS) split_tc_kernel(const LaunchArgs a
   cluster_sync_all();  // no block leaves while another still reads its shared memory
   }  // work items
   if (PERSIST && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
+}
+
+template <class C, bool PERSIST = false, bool FUSED = false>
+__global__ void __launch_bounds__(C::THREADS, FUSED ? C::MINB : 1) split_tc_kernel(const LaunchArgs a) {
+  split_tc_body<C, PERSIST, FUSED>(a);
+}
+
+// The plain per-split kernel of a configuration with a pinned register budget
+// (TcCfg MAXREG_ > 0).
+template <class C>
+__global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXREG) split_tc_kernel_pinned(const LaunchArgs a) {
+  split_tc_body<C, false, false>(a);
 }
 
 // ================================================================ merge kernel
@@ -1403,12 +1445,30 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     return launch_pdl(split_tc_kernel<C, true>, dim3(a.persistent), dim3(C::THREADS), C::SMEM, stream, 1, a);
   }
+  if (a.fused) {
+    e = smem_attr_once<split_tc_kernel<C, false, true>>(static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(split_tc_kernel<C, false, true>, dim3(a.num_splits, a.NKV, a.B), dim3(C::THREADS), C::SMEM,
+                      stream, 1, a);
+  }
   dim3 grid(a.num_splits, a.NKV, a.B);
+  if constexpr (C::MAXREG > 0) {
+    if (a.cluster == 1) {
+      e = smem_attr_once<split_tc_kernel_pinned<C>>(static_cast<int>(C::SMEM));
+      if (e != cudaSuccess) return e;
+      return launch_pdl(split_tc_kernel_pinned<C>, grid, dim3(C::THREADS), C::SMEM, stream, 1, a);
+    }
+  }
   return launch_pdl(split_tc_kernel<C>, grid, dim3(C::THREADS), C::SMEM, stream, a.cluster, a);
 }
 
 template <class C>
 cudaError_t occupancy_tc(int* ctas) {
+  if constexpr (C::MAXREG > 0) {
+    cudaError_t e = smem_attr_once<split_tc_kernel_pinned<C>>(static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel_pinned<C>, C::THREADS, C::SMEM);
+  }
   cudaError_t e = smem_attr_once<split_tc_kernel<C>>(static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_tc_kernel<C>, C::THREADS, C::SMEM);
@@ -1429,8 +1489,8 @@ using Tc128x2 = TcCfg<128, 2, 4, 3>;
 using Tc256x1 = TcCfg<256, 1, 8, 3>;
 using Tc256x2 = TcCfg<256, 2, 8, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;  // a 16-position tile has 8 x 16 softmax slots
-using Tc512x2 = TcCfg<512, 2, 8, 3>;
-using Tc512x2w = TcCfg<512, 2, 8, 3, 4096>;  // one block per SM, 4 KB copies
+using Tc512x2 = TcCfg<512, 2, 8, 3, 2048, false, 96>;      // two blocks per SM (long MQA bands)
+using Tc512x2w = TcCfg<512, 2, 8, 3, 4096, false, 96>;  // one block per SM, 4 KB copies
 // E4M3 caches: a block's copy rate is set by the number of bulk copies it
 // issues, so 2 KB E4M3 groups (the positions of a 4 KB bf16 group) in a
 // two-stage ring, except head dim 256 (small sliding bands), where 1 KB groups
@@ -1445,7 +1505,7 @@ using Tc256x1f = TcCfg<256, 1, 8, 4, 2048, true>;
 using Tc256x2f = TcCfg<256, 2, 8, 4, 2048, true>;
 using Tc512x1f = TcCfg<512, 1, 4, 2, 4096, true>;
 using Tc512x2f = TcCfg<512, 2, 4, 2, 4096, true>;
-using Tc512x2f8 = TcCfg<512, 2, 8, 2, 4096, true>;  // one block per SM
+using Tc512x2f8 = TcCfg<512, 2, 8, 2, 4096, true, 96>;  // one block per SM
 // Head dims 64 and 128 with short bands (the plan's whole-tile splits): 1 KB
 // E4M3 groups in four stages, half the default tile, so a short band spreads
 // over twice as many blocks.

@@ -127,9 +127,10 @@ enum {
  * ~4 MiB per split, before adding waves.
  *
  * Fused merge (opt-in through fd_plan_override; plans use fused = 0): when a
- * group has few partials (G * S <= 480), the last split block of each
- * (sequence, KV head) to finish merges them itself, found with a per-group
- * counter that wraps back to zero; no merge kernel is launched.
+ * group's partials are small (G * S * HS * 4 bytes <= 256 KB), the last split
+ * block of each (sequence, KV head) to finish merges them itself, found with
+ * a per-group counter (one acquire-release atomic per block) that wraps back
+ * to zero; no merge kernel is launched.
  *
  * Copy groups: a tile's K and V rows arrive in groups of about 2 KB, one
  * bulk copy per group. For head dim 512 with more than 8 query rows per KV

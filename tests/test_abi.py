@@ -77,7 +77,7 @@ def test_plan_fills_the_gpu_and_sizes_workspace(name, lib):
     assert p.workspace_zero_bytes == expect_zero
     assert p.fused == 0  # the fused merge is opt-in
     G = w.NH // w.NKV
-    if P > 1 and G * p.num_splits <= 480:
+    if P > 1 and G * p.num_splits * w.HS * 4 <= 256 << 10:
         q = fd.fd_plan_t.from_buffer_copy(p)
         fd.fd_plan_override(q, 0, 0, 0, 1)
         assert q.fused == 1 and q.workspace_bytes == p.workspace_bytes
