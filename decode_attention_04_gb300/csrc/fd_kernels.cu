@@ -1185,7 +1185,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXREG) split_tc_ke
 // ================================================================ merge kernel
 
 constexpr int kMergeWarps = 8;
-constexpr int kMergeBatch = 8;        // partials whose loads one warp issues together
+constexpr int kMergeBatchWide = 20;   // slots per warp per round trip when a row has 64 < S <= 160
 constexpr int kMergeStagedRows = 64;  // rows (B * NH) from which the staged merge is used
 
 // The merge for few rows (B * NH < kMergeStagedRows), where it is one short
@@ -1197,6 +1197,7 @@ constexpr int kMergeStagedRows = 64;  // rows (B * NH) from which the staged mer
 // out = sum_s w_s O_s / sum_s w_s l_s. The first batch of loads goes out
 // with the load of the row's length (every slot is in bounds); slots past
 // the row's active splits are masked once the length has arrived.
+template <int kMergeBatch>  // partials whose loads one warp issues together
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
   __shared__ float sacc[kMergeWarps][32];
   __shared__ float sl[kMergeWarps];
@@ -1686,8 +1687,15 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
   // the fused merge by each group's last block
   if (e != cudaSuccess || a.num_splits == a.cluster || a.fused) return e;
   if (static_cast<long long>(a.B) * a.NH < kMergeStagedRows) {
+    // one round trip of loads per warp: 8 slots each up to 64 partials per
+    // row, 20 up to 160 behind a bf16 cache (measured on GB300, us per layer:
+    // MQA 32k with 152 partials per row 19.7 -> 19.3; behind the E4M3 split
+    // kernel the wide merge lost, 22.5 -> 27.4, so E4M3 keeps rounds of 8)
     dim3 mgrid(a.HS / 32, a.NH, a.B);
-    return launch_pdl(merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+    const int ns = a.num_splits / a.cluster;
+    if (!a.kv8 && ns > kMergeWarps * 8 && ns <= kMergeWarps * kMergeBatchWide)
+      return launch_pdl(merge_kernel<kMergeBatchWide>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+    return launch_pdl(merge_kernel<8>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
   }
   const size_t msmem = merge_smem_bytes(a.num_splits / a.cluster);
   e = smem_attr_once<merge_staged_kernel>(static_cast<int>(merge_smem_bytes(kMergeStageMax)));
