@@ -46,12 +46,12 @@ int slots(const fd_plan_t& p) { return p.num_splits / (p.cluster > 0 ? p.cluster
 
 // Workspace layout:
 //   [counters: B*NKV uint32 split counters when a row has more than one
-//    partial slot, then one work-item counter for a persistent grid; zero
-//    before the first call]
+//    partial slot (followed by B*NKV count-out words for the group step), then
+//    one work-item counter for a persistent grid; zero before the first call]
 //   [O partials: fp32 B*NH*slots*HS] [(m, l): fp32 B*NH*slots*2]   (slots > 1)
 // each part rounded up to 256 bytes.
 long long split_counter_words(const fd_plan_t& p) {
-  return slots(p) > 1 ? static_cast<long long>(p.B) * p.NKV : 0;
+  return slots(p) > 1 ? static_cast<long long>(p.B) * p.NKV * (p.fused == 2 ? 2 : 1) : 0;
 }
 
 size_t ws_counter_bytes(const fd_plan_t& p) {
@@ -99,19 +99,26 @@ int persistent_rule(const fd_plan_t& p) {
   return 0;
 }
 
-// Fused merge (the last split block of each (sequence, KV head) merges) when
-// the group's partials, which that one block reads, stay within 256 KB.
-bool fused_rule_allowed(const fd_plan_t& p) {
+// Fused merge, mode 1 (the last split block of each (sequence, KV head)
+// merges) when the group's partials, which that one block reads, stay within
+// 256 KB; mode 2 (every block of a group waits for the group, then merges a
+// share) when the whole grid is resident at once on the plan's SMs.
+bool fused_rule_allowed(const fd_plan_t& p, int mode = 1) {
   const long long G = p.NH / p.NKV;
-  return p.path == FD_PATH_TC && p.cluster == 1 && slots(p) > 1 &&
-         G * p.num_splits * p.HS * static_cast<long long>(sizeof(float)) <= (256ll << 10);
+  if (p.path != FD_PATH_TC || p.cluster != 1 || slots(p) <= 1) return false;
+  if (mode == 2)
+    return static_cast<long long>(p.B) * p.NKV * p.num_splits <= static_cast<long long>(p.num_sms) * p.ctas_per_sm;
+  return G * p.num_splits * p.HS * static_cast<long long>(sizeof(float)) <= (256ll << 10);
 }
 
-// Off by default: measured on GB300, the separate merge kernel (already
-// resident through programmatic dependent launch) beat the last block's fence,
-// counter and merge on the small bands (ring 7.32 vs 8.95 us per layer, llama
-// tiny 5.89 vs 6.88) and tied on the ragged batch. Kept as an option
-// (fd_plan_override) and tested both ways.
+// Off by default: measured on GB300 (us per layer), the separate merge kernel,
+// whose blocks programmatic dependent launch makes resident early, beat both
+// in-launch forms on the ring (6.14 against 7.27 for the last block, 7.07 for
+// the group step), MQA 4k (8.81 against 11.85 for the group step) and MQA 32k
+// (19.25 against 22.12); only Llama tiny favoured the last block (4.79 against
+// 4.88). Split blocks that wait for their group, or for the last block, hold
+// their SM slots, so the next layer's blocks cannot start early. Kept as
+// options (fd_plan_override) and tested.
 int fused_rule(const fd_plan_t& p) {
   (void)p;
   return 0;
@@ -156,7 +163,7 @@ int warps_rule(const fd_plan_t& p) {
 }
 
 void finish_plan(fd_plan_t* p, int fused = -1, int persistent = -1) {
-  p->fused = fused < 0 ? fused_rule(*p) : (fused && fused_rule_allowed(*p) ? 1 : 0);
+  p->fused = fused < 0 ? fused_rule(*p) : (fused > 0 && fused_rule_allowed(*p, fused) ? fused : 0);
   p->persistent = persistent < 0 ? persistent_rule(*p)
                                  : (persistent && persistent_allowed(*p) ? persistent_blocks(*p) : 0);
   p->group_bytes = group_rule(*p);
@@ -483,7 +490,7 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
   if (cluster > 0) p.cluster = cluster;
   if (p.path == FD_PATH_SIMT && cluster == 0) p.cluster = 1;  // the SIMT path has no clusters
   if (!valid_cluster(p.cluster, p.num_splits, p.HS, p.path)) return FD_ERR_INVALID_ARG;
-  if (fused > 0 && !fused_rule_allowed(p)) return FD_ERR_INVALID_ARG;
+  if (fused > 2 || (fused > 0 && !fused_rule_allowed(p, fused))) return FD_ERR_INVALID_ARG;
   finish_plan(&p, fused);
   *plan = p;
   return FD_OK;
@@ -527,7 +534,7 @@ int check_plan(const fd_plan_t* plan, int kv_dtype, int B, int NH, int NKV, int 
       plan->window != window || plan->kv_dtype != kv_dtype)
     return FD_ERR_INVALID_ARG;
   if (plan->num_splits < 1 || !valid_path(*plan) || plan->granule < 1 || !valid_kv(plan->kv_dtype, plan->path) || !valid_cluster(plan->cluster, plan->num_splits, plan->HS, plan->path) ||
-      (plan->fused && !fused_rule_allowed(*plan)))
+      plan->fused < 0 || plan->fused > 2 || (plan->fused && !fused_rule_allowed(*plan, plan->fused)))
     return FD_ERR_INVALID_ARG;
   if (plan->min_len < 0) return FD_ERR_INVALID_ARG;
   if (plan->persistent < 0 ||

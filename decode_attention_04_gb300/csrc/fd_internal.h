@@ -20,10 +20,12 @@ struct LaunchArgs {
   const int* lens;          // int32 [B]
   float* ws_o;              // fp32 [B][NH][S][HS]  (S > 1 only)
   float* ws_ml;             // fp32 [B][NH][S][2]   (m in log2 units, l)
-  unsigned int* counters;   // [B][NKV] finished-split counters (fused merge), zero between calls
+  unsigned int* counters;   // [B][NKV] finished-split counters (fused merge), zero between calls;
+                            // with the group step, [B][NKV] count-out words after them
   unsigned int* work_counter;  // persistent grid: next work item, zero between calls
   int persistent;           // blocks of a persistent split grid; 0: one block per split
-  int fused;                // 1: the last split block of each (b, kvh) merges; no merge kernel
+  int fused;                // 1: the last split block of each (b, kvh) merges; 2: every split block
+                            // of a group waits for the group, then merges a share; no merge kernel
   int group_bytes;          // bytes per bulk-copy group of the tile (2048, or 4096 for the wide MQA tile)
   int consumer_warps;       // consumer warps of the split tile (the plan's choice)
   int kv8;                  // 1: the cache is E4M3 codes (k8/v8) with per-(b, kvh) scales

@@ -246,14 +246,16 @@ struct TcCfg {
   static constexpr int MP = T / 16;       // 16-row MMA tiles per pipeline tile
   static constexpr int PPITCH = T + 8;    // P row pitch (bf16)
   static constexpr int TPR = CTHREADS / NP;  // softmax threads per query row
-  static constexpr int PPT = T / TPR;        // positions per softmax thread
   // E4M3 tiles with at most NP / 2 real query rows: twice the threads per row
   // (one warp at most) and half the positions each, so the softmax skips the
   // padded rows and each warp reads one row of scores (no bank conflicts).
   // Measured on GB300 (us per layer): E4M3 Llama ragged 152.3 -> 140.8,
   // tiny 5.70 -> 5.62; the bf16 tiles lost (ragged 159.4 -> 163.2), so they
-  // keep the full mapping.
-  static constexpr int TPR2 = (KV8 && 2 * TPR <= 32 && T % (2 * TPR) == 0) ? 2 * TPR : TPR;
+  // keep the full mapping. Head dim 512 keeps it too: its tiles serve 16-row
+  // MQA groups, and the second mapping compiled into them alone cost E4M3
+  // MQA long 123.6 -> 128.3 and MQA 32k 21.7 -> 22.5.
+  static constexpr int TPR2 =
+      (KV8 && HS <= 256 && 2 * TPR <= 32 && T % (2 * TPR) == 0) ? 2 * TPR : TPR;
   static constexpr size_t STAGE_BYTES = static_cast<size_t>(NG) * GP;
   // bf16 tiles held: the copy ring itself, or none (KV8 reads its own ring)
   static constexpr int NBUF = KV8 ? 0 : NSTAGE;
@@ -385,11 +387,6 @@ __device__ __forceinline__ void produce_tile(const LaunchArgs& a, const unsigned
   }
 }
 
-// A producer warp's last step: wait (bounded, with its own failure flag) for
-// the last phase it issued into each stage of the ring, so no copy of this
-// block is still in flight when the block exits. Earlier phases of a stage
-// completed before that stage was issued again, and only the producers
-// arrive on the full barriers, so the last issued phase is the last phase.
 // Atomic increment with wrap ((old >= limit) ? 0 : old + 1) and
 // acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned* p, unsigned limit) {
@@ -398,6 +395,24 @@ __device__ __forceinline__ unsigned atom_inc_acq_rel(unsigned* p, unsigned limit
   return old;
 }
 
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+
+// A producer warp's last step: wait (bounded, with its own failure flag) for
+// the last phase it issued into each stage of the ring, so no copy of this
+// block is still in flight when the block exits. Earlier phases of a stage
+// completed before that stage was issued again, and only the producers
+// arrive on the full barriers, so the last issued phase is the last phase.
 template <class C>
 __device__ __forceinline__ void producer_drain(uint32_t full0, uint32_t st_issued, uint32_t st_par) {
   bool dfail = false;
@@ -406,12 +421,17 @@ __device__ __forceinline__ void producer_drain(uint32_t full0, uint32_t st_issue
     if ((st_issued >> st) & 1u) mbar_wait(full0 + 8 * st, (st_par >> st) & 1u, dfail);
 }
 
-// The split kernel's body. PERSIST: the persistent grid; FUSED: the last block
-// of each group merges. Each is a separate instance, so the plain per-split
+constexpr int kFusedLast = 1;   // fd_plan_t.fused values
+constexpr int kFusedGroup = 2;
+
+// The split kernel's body. PERSIST: the persistent grid; FUSED: the merge in
+// the split launch (kFusedLast: the last block of each group merges;
+// kFusedGroup: every block of a group waits for the group, then merges a
+// share of its outputs). Each is a separate instance, so the plain per-split
 // kernel keeps its registers (on GB300 every register it gains can keep the
 // merge kernel's blocks, which wait beside it under programmatic dependent
 // launch, off the SM).
-template <class C, bool PERSIST, bool FUSED>
+template <class C, bool PERSIST, int FUSED>
 __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_seq[kLptMaxB];
@@ -808,7 +828,7 @@ __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
       const float alpha = (m_new == kNegInf) ? 1.f : exp2f(m_run - m_new);
       float psum = 0.f;
       uint16_t* phi = sP + sr * C::PPITCH;
-      uint16_t* plo = sP + (C::NP + sr) * C::PPITCH;
+      [[maybe_unused]] uint16_t* plo = sP + (C::NP + sr) * C::PPITCH;  // bf16 tiles: the low halves of P
 #pragma unroll
       for (int t = 0; t < PPTx; ++t) {
         const int j = sj + t * TPRx;
@@ -980,6 +1000,132 @@ __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
     }
     if constexpr (!FUSED) continue;
     if (direct) continue;
+
+    if constexpr (FUSED == kFusedGroup) {
+      // ---- group step: every active block of this (sequence, KV head) counts
+      // in, waits until the whole group has, then merges its share of the
+      // group's G x HS outputs. The grid is launched cooperatively (every
+      // block resident at once), so the wait ends; it is bounded all the
+      // same. Thread 0 counts the block in with an acquire-release add (the
+      // barrier before it orders the block's partial stores first), so the
+      // last arrival has observed every partial, and waits with acquire loads
+      // until the count is complete, which passes that view on (and, through
+      // the barrier after the wait, to the block). Each block then counts out
+      // on a second word; the last one out sets both words back to zero for
+      // the next call (every other block has seen the full count by then).
+      __shared__ int s_go;
+      unsigned* cnt = a.counters + static_cast<size_t>(b) * a.NKV + kvh;
+      unsigned* out_cnt = cnt + static_cast<size_t>(a.B) * a.NKV;
+      named_bar_sync(1, C::CTHREADS);
+      if (tid == 0) {
+        int go = 1;
+        const unsigned need = static_cast<unsigned>(nact);
+        if (atom_add_acq_rel(cnt, 1u) + 1u < need) {
+          uint64_t t0 = 0;
+          for (uint32_t i = 1; ld_acquire_u32(cnt) < need; ++i) {
+            if ((i & 255u) != 0) continue;  // the clock is read every 256 polls
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+              t0 = now;
+            } else if (now - t0 > g_wait_limit_ns) {
+              go = 0;
+              atomicOr(&g_device_error, FD_DEVERR_WAIT_TIMEOUT);
+              break;
+            }
+          }
+        }
+        if (go && atomicAdd(out_cnt, 1u) == need - 1u) {
+          *reinterpret_cast<volatile unsigned*>(cnt) = 0u;
+          *reinterpret_cast<volatile unsigned*>(out_cnt) = 0u;
+        }
+        s_go = go;
+      }
+      named_bar_sync(1, C::CTHREADS);
+      if (!s_go) return;
+
+      // Block s of the nact active ones takes items [s * per, (s + 1) * per)
+      // of the group's (row, 4 dims) items. A warp takes 32 / LG items at
+      // once, LG lanes each (the power of two >= nact, at most 32); the lanes
+      // of an item take its slots sl, sl + LG, ... with every load in flight
+      // at once, fold them online, and combine with a butterfly inside the
+      // LG lanes, which gives each of them the same, order-fixed sum.
+      const int S = a.num_splits;
+      constexpr int D4 = C::HS / 4;
+      constexpr int kLoads = 8;  // slots per lane per round trip
+      const int items = G * D4;
+      const int per = (items + nact - 1) / nact;
+      const int i_end = min(items, (s + 1) * per);
+      int LG = 1;
+      while (LG < nact && LG < 32) LG <<= 1;
+      const int ipw = 32 / LG, sub = lane / LG, sl = lane % LG;
+      for (int it0 = s * per + warp * ipw; it0 < i_end; it0 += C::NWC * ipw) {
+        const int it = min(it0 + sub, i_end - 1);  // lanes past the end repeat the last item, unstored
+        const int g = it / D4, d = (it % D4) * 4;
+        const size_t row = static_cast<size_t>(b) * a.NH + hbase + g;
+        const float4* src = reinterpret_cast<const float4*>(a.ws_o + row * S * C::HS + d);
+        const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + row * S;
+        float M = kNegInf, L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j0 = sl; j0 < nact; j0 += LG * kLoads) {
+          float4 v[kLoads];
+          float2 w2[kLoads];
+#pragma unroll
+          for (int u = 0; u < kLoads; ++u) {
+            const int j = j0 + LG * u;
+            v[u] = j < nact ? __ldcg(src + static_cast<size_t>(j) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            w2[u] = j < nact ? __ldcg(ml + j) : make_float2(kNegInf, 0.f);
+          }
+          float bm = kNegInf;
+#pragma unroll
+          for (int u = 0; u < kLoads; ++u) bm = fmaxf(bm, w2[u].x);
+          const float mn = fmaxf(M, bm);
+          if (mn == kNegInf) continue;
+          const float sc = exp2f(M - mn);  // 0 while M is still -inf
+          L *= sc;
+          acc.x *= sc;
+          acc.y *= sc;
+          acc.z *= sc;
+          acc.w *= sc;
+#pragma unroll
+          for (int u = 0; u < kLoads; ++u) {
+            const float w = exp2f(w2[u].x - mn);  // 0 for padding and empty partials; NaN for a NaN m
+            L += w * w2[u].y;
+            acc.x += w * v[u].x;
+            acc.y += w * v[u].y;
+            acc.z += w * v[u].z;
+            acc.w += w * v[u].w;
+          }
+          M = mn;
+        }
+        for (int off = LG >> 1; off > 0; off >>= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, off);
+          const float Lo = __shfl_xor_sync(0xffffffffu, L, off);
+          const float4 ao = make_float4(__shfl_xor_sync(0xffffffffu, acc.x, off),
+                                        __shfl_xor_sync(0xffffffffu, acc.y, off),
+                                        __shfl_xor_sync(0xffffffffu, acc.z, off),
+                                        __shfl_xor_sync(0xffffffffu, acc.w, off));
+          const float mn = fmaxf(M, Mo);
+          const float sa = M == kNegInf ? 0.f : exp2f(M - mn);
+          const float sb = Mo == kNegInf ? 0.f : exp2f(Mo - mn);
+          L = L * sa + Lo * sb;
+          acc.x = acc.x * sa + ao.x * sb;
+          acc.y = acc.y * sa + ao.y * sb;
+          acc.z = acc.z * sa + ao.z * sb;
+          acc.w = acc.w * sa + ao.w * sb;
+          M = mn;
+        }
+        if (sl == 0 && it0 + sub < i_end) {
+          const float4 val = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+          const uint32_t lo2 = static_cast<uint32_t>(f32_to_bf16_bits(val.x)) |
+                               (static_cast<uint32_t>(f32_to_bf16_bits(val.y)) << 16);
+          const uint32_t hi2 = static_cast<uint32_t>(f32_to_bf16_bits(val.z)) |
+                               (static_cast<uint32_t>(f32_to_bf16_bits(val.w)) << 16);
+          *reinterpret_cast<uint2*>(a.out + row * C::HS + d) = make_uint2(lo2, hi2);
+          if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + row * C::HS + d) = val;
+        }
+      }
+      return;
+    }
 
     // ---- fused merge: the last block of this (sequence, KV head) to finish
     // combines every partial of the group (no merge launch). Thread 0 counts
@@ -1170,7 +1316,7 @@ __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
   if (PERSIST && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
 }
 
-template <class C, bool PERSIST = false, bool FUSED = false>
+template <class C, bool PERSIST = false, int FUSED = 0>
 __global__ void __launch_bounds__(C::THREADS, FUSED ? C::MINB : 1) split_tc_kernel(const LaunchArgs a) {
   split_tc_body<C, PERSIST, FUSED>(a);
 }
@@ -1429,6 +1575,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The same with every block of the grid resident at once (a cooperative
+// launch: the driver refuses a grid that cannot be), for kernels whose blocks
+// wait on one another.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Kernel attributes are set once per (kernel, device): the values never
 // change, and the driver call would otherwise sit on every launch's host path.
 template <auto Kernel>
@@ -1471,11 +1638,17 @@ cudaError_t launch_tc(const LaunchArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     return launch_pdl(split_tc_kernel<C, true>, dim3(a.persistent), dim3(C::THREADS), C::SMEM, stream, 1, a);
   }
-  if (a.fused) {
-    e = smem_attr_once<split_tc_kernel<C, false, true>>(static_cast<int>(C::SMEM));
+  if (a.fused == kFusedGroup) {
+    e = smem_attr_once<split_tc_kernel<C, false, kFusedGroup>>(static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
-    return launch_pdl(split_tc_kernel<C, false, true>, dim3(a.num_splits, a.NKV, a.B), dim3(C::THREADS), C::SMEM,
-                      stream, 1, a);
+    return launch_pdl_cooperative(split_tc_kernel<C, false, kFusedGroup>, dim3(a.num_splits, a.NKV, a.B),
+                                  dim3(C::THREADS), C::SMEM, stream, a);
+  }
+  if (a.fused) {
+    e = smem_attr_once<split_tc_kernel<C, false, kFusedLast>>(static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(split_tc_kernel<C, false, kFusedLast>, dim3(a.num_splits, a.NKV, a.B), dim3(C::THREADS),
+                      C::SMEM, stream, 1, a);
   }
   dim3 grid(a.num_splits, a.NKV, a.B);
   if constexpr (C::MAXREG > 0) {

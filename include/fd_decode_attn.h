@@ -126,11 +126,19 @@ enum {
  * in a split: then it fills every resident block slot once, with up to
  * ~4 MiB per split, before adding waves.
  *
- * Fused merge (opt-in through fd_plan_override; plans use fused = 0): when a
- * group's partials are small (G * S * HS * 4 bytes <= 256 KB), the last split
- * block of each (sequence, KV head) to finish merges them itself, found with
- * a per-group counter (one acquire-release atomic per block) that wraps back
- * to zero; no merge kernel is launched.
+ * Fused merge (opt-in through fd_plan_override; plans use fused = 0), two
+ * forms, neither launching the merge kernel:
+ *   fused = 1, the last block: when a group's partials are small
+ *   (G * S * HS * 4 bytes <= 256 KB), the last split block of each (sequence,
+ *   KV head) to finish merges them itself, found with a per-group counter
+ *   (one acquire-release atomic per block) that wraps back to zero.
+ *   fused = 2, the group step: when the whole grid is resident at once
+ *   (B * NKV * S <= num_sms * ctas_per_sm), the grid is launched
+ *   cooperatively; every active split block of a group counts in on the same
+ *   counter, waits (bounded) until the whole group has, then merges its
+ *   share of the group's G x HS outputs, and counts out on a second word
+ *   (B * NKV more workspace words after the counters); the last block out
+ *   sets both back to zero.
  *
  * Copy groups: a tile's K and V rows arrive in groups of about 2 KB, one
  * bulk copy per group. For head dim 512 with more than 8 query rows per KV
@@ -168,7 +176,7 @@ typedef struct {
   int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
   int num_sms;             /* SM count the plan assumed */
   int max_cluster;         /* largest cluster the device schedules for this kernel */
-  int fused;               /* 1: each group's last split block merges (no merge kernel) */
+  int fused;               /* 1: each group's last split block merges; 2: the group step (no merge kernel) */
   int group_bytes;         /* bytes per bulk-copy group of a tile: 2048 or 4096 (bf16); 2048 or 1024 (E4M3) */
   int kv_dtype;            /* FD_KV_BF16 or FD_KV_E4M3: the cache type the plan was made for */
   int consumer_warps;      /* MMA warps per split block (2, 4 or 8; 0 on the SIMT path) */
@@ -220,7 +228,8 @@ int fd_plan_sms_kv(int B, int NH, int NKV, int HS, int capacity, int window, int
  * shapes above), the cluster size
  * (cluster >= 1, a power of two <= 16 that divides num_splits and HS / 4;
  * 0 keeps the plan's; the SIMT path takes cluster 1 only) and/or the fused
- * merge (fused = 0 off, 1 on where allowed, -1 the plan's rule), then
+ * merge (fused = 0 off, 1 the last block, 2 the group step, each where
+ * allowed; -1 the plan's rule), then
  * recompute the dependent fields (fused, group_bytes, workspace sizes). Used
  * to test that the result does not depend on these choices, and to bisect.
  * Errors: FD_ERR_INVALID_ARG.
@@ -271,7 +280,8 @@ int fd_plan_min_len(fd_plan_t* plan, int min_len);
 
 /*
  * fd_workspace_bytes: workspace a plan needs. With P = num_splits / cluster
- * partial slots per row: when P > 1, B * NKV 32-bit split counters; with a
+ * partial slots per row: when P > 1, B * NKV 32-bit split counters (twice
+ * that with the group step, fused = 2); with a
  * persistent grid, one more 32-bit work-item counter; when P > 1, then
  * B * NH * P * HS fp32 partial outputs and B * NH * P * 2 fp32 (m, l). Each
  * part is rounded up to 256 bytes. 0 when P == 1 without a persistent grid

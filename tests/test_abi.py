@@ -434,3 +434,37 @@ def test_plan_min_len_recorded_and_checked(lib):
     assert lib.fd_plan_min_len(ctypes.byref(p), -1) == fd.FD_ERR_INVALID_ARG
     assert lib.fd_plan_min_len(None, 5) == fd.FD_ERR_INVALID_ARG
     assert p.min_len == w.capacity
+
+
+def test_group_step_plan_rules(lib):
+    """fused = 2 (the group step): allowed on the tensor-core path without
+    clusters when the whole grid is resident at once (B * NKV * S <= SMs x
+    CTAs per SM); the counter region doubles (count-in and count-out words,
+    both zeroed); refused beyond one wave, with clusters, with the persistent
+    grid, and for fused values other than -1..2."""
+    up = lambda x: -(-x // 256) * 256
+    w = WORKLOADS["gemma_local_ring"]
+    p = _plan(w)  # 152 SMs x 2 CTAs
+    q = fd.fd_plan_t.from_buffer_copy(p)
+    fd.fd_plan_override(q, 0, 0, 0, 2)
+    assert q.fused == 2 and q.num_splits == p.num_splits
+    assert q.workspace_zero_bytes == up(2 * w.B * w.NKV * 4)
+    assert q.workspace_bytes == p.workspace_bytes - p.workspace_zero_bytes + q.workspace_zero_bytes
+    assert q.workspace_bytes == fd.fd_workspace_bytes(q)
+    cap = 152 * 2 // (w.B * w.NKV)
+    fd.fd_plan_override(q, cap, 0, 0, 2)
+    assert q.fused == 2
+    for args in [(cap + 1, 0, 1, 2), (32, 0, 2, 2), (0, fd.FD_PATH_SIMT, 0, 2), (0, 0, 0, 3)]:
+        with pytest.raises(fd.FdError):
+            fd.fd_plan_override(fd.fd_plan_t.from_buffer_copy(p), *args)
+    with pytest.raises(fd.FdError):
+        fd.fd_plan_persistent(q, 1)
+    fd.fd_plan_override(q, 0, 0, 0, 0)
+    assert q.fused == 0 and q.workspace_bytes == fd.fd_workspace_bytes(q)
+    # a hand-edited plan with an unknown mode is refused before any launch
+    bad = fd.fd_plan_t.from_buffer_copy(p)
+    bad.fused = 3
+    dummy = ctypes.c_void_p(256)
+    rc = lib.fd_decode_attn_ex(ctypes.byref(bad), dummy, bad.workspace_bytes, None, dummy, dummy, dummy, dummy,
+                               dummy, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
+    assert rc == fd.FD_ERR_INVALID_ARG

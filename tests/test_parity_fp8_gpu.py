@@ -53,6 +53,10 @@ def test_fp8_fused_merge_and_clusters_agree_with_the_oracle():
     q, k8, v8, ks, vs, lens = make_inputs_fp8(w)
     ref = oracle_ref_fp8(w, q, k8, v8, ks, vs, lens)
     check(run_fp8(w, q, k8, v8, ks, vs, lens, splits=8, fused=1), ref, what="fused")
+    for S in (2, 8, 32):
+        res = run_fp8(w, q, k8, v8, ks, vs, lens, splits=S, fused=2)
+        assert res["plan"].fused == 2
+        check(res, ref, what=f"group step S={S}")
     check(run_fp8(w, q, k8, v8, ks, vs, lens, splits=8, cluster=8), ref, what="one cluster")
     check(run_fp8(w, q, k8, v8, ks, vs, lens, splits=16, cluster=4), ref, what="clusters of 4")
 

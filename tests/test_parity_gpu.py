@@ -114,6 +114,79 @@ def test_fused_merge_equals_merge_kernel(w):
         assert (outs[0] - outs[1]).abs().max().item() <= 1e-5
 
 
+GROUP_CASES = FUSED_CASES + [
+    W("gs_mqa_many_splits", 1, 16, 1, 512, 32768, 0, lens=(20000,), seed=74),
+    W("gs_llama_tiny", 1, 32, 8, 128, 512, 0, lens=(256,), seed=75),
+    W("gs_ring_not_full", 1, 16, 8, 256, 1024, 1024, lens=(700,), seed=76),
+    W("gs_window_chunks", 2, 16, 8, 256, 1024, 300, lens=(5000, 299), seed=77),
+]
+
+
+@pytest.mark.parametrize("w", GROUP_CASES, ids=[c.name for c in GROUP_CASES])
+def test_group_step_merge_matches_oracle_and_merge_kernel(w):
+    """fused = 2: every split block of a group waits for the group inside the
+    (cooperative) split launch, then merges a share of the outputs. Agrees with
+    the oracle and with the merge kernel at every split count the grid allows
+    (one wave), is bit-identical run to run, and leaves both counter words at
+    zero."""
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    s_cap = plan.num_sms * plan.ctas_per_sm // (w.B * w.NKV)
+    assert s_cap >= 2
+    for S in sorted(x for x in {2, 3, 8, 19, 32, 38, 76, s_cap} if x <= s_cap):
+        base = run(w, q, k, v, lens, splits=S, cluster=1, fused=0)
+        res = run(w, q, k, v, lens, splits=S, cluster=1, fused=2)
+        assert res["plan"].fused == 2
+        assert res["plan"].workspace_zero_bytes >= 2 * 4 * w.B * w.NKV
+        check(res, ref, what=f"{w.name} S={S} group step")
+        assert res["deverr"] & fd.FD_DEVERR_WAIT_TIMEOUT == 0
+        assert (res["out32"] - base["out32"]).abs().max().item() <= 1e-5
+        again = run(w, q, k, v, lens, splits=S, cluster=1, fused=2)
+        assert torch.equal(again["out32"], res["out32"])
+    with pytest.raises(fd.FdError):  # a grid beyond one wave cannot wait on itself
+        fd.fd_plan_override(fd.fd_plan_t.from_buffer_copy(plan), s_cap + 1, 0, 1, 2)
+
+
+def test_group_step_graph_replays_reuse_the_counters():
+    """A captured group-step call replayed with new lengths: every replay is
+    exact (the counter words return to zero each time), and the E4M3 cache
+    takes the same step."""
+    w = W("gs_graph", 1, 16, 8, 256, 1024, 1024, lens=(5000,), seed=78)
+    q, k, v, lens = make_inputs(w)
+    dev = torch.device("cuda")
+    qd, kd, vd, ld = q.to(dev), k.to(dev), v.to(dev), lens.to(dev)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    fd.fd_plan_override(plan, 0, 0, 1, 2)
+    assert plan.fused == 2
+    ws = torch.zeros(max(16, plan.workspace_bytes), dtype=torch.uint8, device=dev)
+    o16 = Guarded(w.B * w.NH * w.HS * 2, dev, fill=0xFF)
+    o32 = Guarded(w.B * w.NH * w.HS * 4, dev, fill=0xFF)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside the capture
+        fd.fd_decode_attn_ex(plan, ws, plan.workspace_bytes, o32.ptr(), qd, kd, vd, o16.ptr(), ld, w.B, w.NH,
+                             w.NKV, w.HS, w.capacity, w.window, w.scale)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):  # three calls in a row on one workspace
+            fd.fd_decode_attn_ex(plan, ws, plan.workspace_bytes, o32.ptr(), qd, kd, vd, o16.ptr(), ld, w.B,
+                                 w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+    fd.fd_get_device_error()
+    for new_len in (3000, 1024, 700, 1, 5000):
+        ld.fill_(new_len)
+        g.replay()
+        torch.cuda.synchronize()
+        res = dict(out=o16.view(torch.bfloat16, (w.B, w.NH, w.HS)).cpu(),
+                   out32=o32.view(torch.float32, (w.B, w.NH, w.HS)).cpu(),
+                   counters_zero=bool((ws[: plan.workspace_zero_bytes] == 0).all().item()),
+                   canaries=o16.canaries_intact() and o32.canaries_intact())
+        check(res, oracle_ref(w, q, k, v, torch.tensor([new_len], dtype=torch.int32)),
+              what=f"group step replay, len {new_len}")
+    assert fd.fd_get_device_error() == 0
+
+
 CLUSTER_CASES = [
     W("cl_mqa", 2, 16, 1, 512, 700, 0, lens=(700, 3), seed=61),
     W("cl_ring", 1, 16, 8, 256, 256, 200, lens=(1234,), seed=62),
