@@ -483,7 +483,10 @@ int fd_plan_override(fd_plan_t* plan, int num_splits, int path, int cluster, int
   fd_plan_t p = *plan;
   if (path != FD_PATH_AUTO && path != p.path) {
     p.path = path;
-    p.granule = 1;  // a forced kernel family walks single-position chunks
+    // a forced kernel family walks single-position chunks; the tensor-memory
+    // kernel 16-position ones (one P.V step), so only the band's last split
+    // has rows that do not fill its boxes or its last P.V step
+    p.granule = path == FD_PATH_UMMA ? 16 : 1;
   }
   if (!valid_kv(p.kv_dtype, p.path) || !valid_path(p)) return FD_ERR_INVALID_ARG;
   if (num_splits > 0) p.num_splits = num_splits;

@@ -9,21 +9,24 @@
 //     are always [0, min(len, capacity)): a split takes the consecutive slots
 //     [s * chunk, (s + 1) * chunk) of that range (the softmax does not depend
 //     on the order of positions), in tiles of 128.
-//   * Warp 0 streams K and warp 1 streams V as TMA boxes (128-byte swizzle,
-//     64 head dims wide) into two separate rings: K in 16 KB chunks (128
-//     positions x 64 dims), V in 32 KB pairs of chunks (128 dims, one P.V
-//     MMA block). Boxes are 128, 64, 32, 16 or 8 rows high, so a tile's rows
-//     are read exactly; the last rows of a slice that do not fill 8 are loaded
-//     by the producer warp's lanes (all of a tile's at once) and stored into
-//     the same swizzled layout. Nothing outside the band is read.
-//   * Warp 2 owns the tensor memory and issues every MMA from one thread, out
+//   * Warp 0 streams K and V as TMA boxes (128-byte swizzle, 64 head dims
+//     wide) through one ring of 32 KB slots, each a pair of chunks (128
+//     positions x 128 dims: one P.V MMA block, or two K chunks). The stream
+//     order is K(0), then V(i) and K(i + 1) pair by pair, then the last
+//     tile's V: V(i) is requested while K(i + 1) streams, so it lands about
+//     when P(i) is ready instead of holding slots through the softmax, and
+//     the scores of tile i + 1 never wait for V. Boxes are 128, 64, 32, 16
+//     or 8 rows high, so a tile's rows are read exactly; the last rows of a
+//     slice that do not fill 8 are loaded by the copy warp's lanes and stored
+//     into the same swizzled layout. Nothing outside the band is read.
+//   * Warp 1 owns the tensor memory and issues every MMA from one thread, out
 //     of order between two streams: S^T (128 positions x 16 rows, fp32) =
 //     K Q^T as each K chunk lands (4 MMAs of K = 16 dims per chunk, into one
 //     of two S buffers), and O^T (512 dims x 16 rows) += V^T P^T for tile i
 //     once P(i) is ready and each V pair lands (P = hi + lo bf16, ~16 bits of
 //     each weight). The scores of tile i + 1 are therefore computed while the
 //     softmax of tile i runs, and the K stream never waits for V.
-//   * Warps 3-6 read S from tensor memory (one position per thread), take the
+//   * Warps 2-5 read S from tensor memory (one position per thread), take the
 //     tile's row maxima with a halving butterfly (16 shuffles for 16 rows) and
 //     one barrier, and write P. The running maximum moves only when a row's
 //     tile maximum exceeds it by more than 2^8 (then O is rescaled in tensor
@@ -31,7 +34,7 @@
 //     2^8, are taken against the old maximum, which gives the same softmax.
 //     Row sums stay per thread until the end: one reduction per split.
 //
-// All waits are bounded (fd_device.cuh); the copy warps wait for their last
+// All waits are bounded (fd_device.cuh); the copy warp waits for its last
 // copies and the MMA warp for its last MMAs before the block leaves, and the
 // tensor memory is released on every path that allocated it.
 
@@ -57,35 +60,41 @@ constexpr int T = 128;                    // positions per tile: the score MMA's
 constexpr int DC = 64;                    // head dims per chunk: one 128-byte swizzle row
 constexpr int NCH = HS / DC;              // chunks per tensor per tile
 constexpr int CHUNK_BYTES = T * DC * 2;   // one 128-row TMA box: 16 KB
-constexpr int PAIR_BYTES = 2 * CHUNK_BYTES;
-constexpr int NK = 5;                     // K ring: chunks
-constexpr int NVP = 3;                    // V ring: chunk pairs (128 dims: one P.V MMA block)
-constexpr int MAX_TAIL = NCH * 7 * 8 / 32;  // 16-byte tail pieces per lane (at most 7 rows)
+constexpr int PAIR_BYTES = 2 * CHUNK_BYTES;  // 128 positions x 128 dims: one ring slot
+constexpr int NPAIR = NCH / 2;            // pairs per tensor per tile
+constexpr int NPS = 6;                    // ring slots (pairs), K and V alike
+constexpr int MAX_TAIL = (NCH * 7 * 8 + 31) / 32;  // 16-byte tail pieces per lane (a tile's tensor, at most 7 rows)
 constexpr int NMAP = 5;                   // box heights T, T/2, T/4, T/8, T/16 (= 8)
 constexpr int NSOFT = 4;                  // softmax warps, one TMEM lane quarter each
-constexpr int W_K = 0, W_V = 1, W_MMA = 2, W_SOFT0 = 3;
+constexpr int W_COPY = 0, W_MMA = 1, W_SOFT0 = 2;
 constexpr int THREADS = (W_SOFT0 + NSOFT) * 32;
 constexpr int ATOM_Q = NQ * 128;          // 16 rows x 128 B: one K-major swizzle column of Q or P
 constexpr int P_HALF = (T / 64) * ATOM_Q; // T positions of one half (hi or lo)
 constexpr int P_BUF = 2 * P_HALF;         // hi + lo
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + NK * CHUNK_BYTES;
-constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;   // Q: NCH atoms of 16 rows x 64 dims
-constexpr int OFF_P = OFF_Q + NCH * ATOM_Q;       // P: [2 buffers][hi, lo][T / 64 atoms]
-constexpr int OFF_RED = OFF_P + 2 * P_BUF;        // f32 [2][NQ][NSOFT] tile maxima, [NQ][NSOFT] sums
+constexpr int OFF_RING = 0;
+constexpr int OFF_Q = OFF_RING + NPS * PAIR_BYTES;  // Q: NCH atoms of 16 rows x 64 dims
+constexpr int OFF_P = OFF_Q + NCH * ATOM_Q;         // P: [2 buffers][hi, lo][T / 64 atoms]
+constexpr int OFF_RED = OFF_P + 2 * P_BUF;          // f32 [2][NQ][NSOFT] tile maxima, [NQ][NSOFT] sums
 constexpr int RED_FLOATS = 3 * NQ * NSOFT;
 constexpr int OFF_BAR = OFF_RED + RED_FLOATS * 4;
-// full_k[NK], empty_k[NK], full_v[NVP], empty_v[NVP], s_full[2], s_free[2],
-// p_ready[2], pv_done[2], q_ready, mma_done
-constexpr int NBAR = 2 * NK + 2 * NVP + 8 + 2;
+// full[NPS], empty[NPS], s_full[2], s_free[2], p_ready[2], pv_done[2], q_ready, mma_done
+constexpr int NBAR = 2 * NPS + 8 + 2;
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;      // u32: tensor memory base address
 constexpr int SMEM = OFF_TMEM + 16 + 1024;        // + slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 128;               // S[2] at columns 0, 16; O block mb at 32 + 16 mb
 constexpr float kRescaleLog2 = 8.f;               // the running max moves when a tile's exceeds it by 2^8
 
 static_assert(SMEM <= 227 * 1024, "shared memory");
-static_assert(OFF_V % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
+static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0, "swizzle atoms are 1024-byte aligned");
 static_assert((T >> (NMAP - 1)) == 8, "smallest box: 8 rows (1024 bytes, one swizzle atom)");
+static_assert(MAX_TAIL * 32 >= NCH * 7 * 8, "every tail piece of a tile's tensor has a lane");
+
+// The one copy stream: K(0), then V(i) and K(i + 1) pair by pair, then the
+// last tile's V. Stream position of each pair (ring slot = position % NPS).
+__device__ __forceinline__ int seq_k(int t, int p) { return t == 0 ? p : NPAIR + 2 * NPAIR * (t - 1) + 2 * p + 1; }
+__device__ __forceinline__ int seq_v(int t, int p, int ntiles) {
+  return NPAIR + 2 * NPAIR * t + (t + 1 < ntiles ? 2 * p : p);
+}
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5 = 1), A and
 // B bf16 (bits 7-9, 10-12 = 1), A MN-major when bit 15 is set, N / 8 at bits
@@ -244,21 +253,16 @@ __global__ void __launch_bounds__(um::THREADS, 1)
   const int hbase = kvh * G;
 
   const uint32_t bar0 = base + OFF_BAR;
-  const uint32_t full_k = bar0, empty_k = full_k + 8 * NK;
-  const uint32_t full_v = empty_k + 8 * NK, empty_v = full_v + 8 * NVP;
-  const uint32_t s_full = empty_v + 8 * NVP, s_free = s_full + 16, p_ready = s_free + 16, pv_done = p_ready + 16;
+  const uint32_t full = bar0, empty = full + 8 * NPS;
+  const uint32_t s_full = empty + 8 * NPS, s_free = s_full + 16, p_ready = s_free + 16, pv_done = p_ready + 16;
   const uint32_t q_ready = pv_done + 16, mma_done = q_ready + 8;
   float* red = reinterpret_cast<float*>(smem + OFF_RED);
 
   // Set-up that reads no input, overlapping the previous kernel's tail.
   if (tid == 0) {
-    for (int k = 0; k < NK; ++k) {
-      mbar_init(full_k + 8 * k, 1);   // the copy warp's arrival + the bytes
-      mbar_init(empty_k + 8 * k, 1);  // one tcgen05.commit
-    }
-    for (int k = 0; k < NVP; ++k) {
-      mbar_init(full_v + 8 * k, 1);
-      mbar_init(empty_v + 8 * k, 1);
+    for (int k = 0; k < NPS; ++k) {
+      mbar_init(full + 8 * k, 1);   // the copy warp's arrival + the bytes
+      mbar_init(empty + 8 * k, 1);  // one tcgen05.commit
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(s_full + 8 * j, 1);
@@ -270,25 +274,7 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
-  if ((warp == W_K || warp == W_V) && lane == 0) {
-    const bool is_k = warp == W_K;
-#pragma unroll
-    for (int i = 0; i < NMAP; ++i) prefetch_tensor_map(is_k ? &maps.k[i] : &maps.v[i]);
-    // This split's first tile of the slots [0, min(min_len, capacity)),
-    // which every allowed length makes live: ask L2 for it while the previous
-    // kernel runs (a hint only; the copies come after the dependency wait).
-    const int band_min = min(max(a.min_len, 0), a.capacity);
-    if (band_min > 0) {
-      const int cmin = chunk_of(band_min, S, a.granule);
-      const long long p0 = static_cast<long long>(s) * cmin;
-      if (p0 < band_min) {
-        const int nmin =
-            static_cast<int>(min(static_cast<long long>(T), min(static_cast<long long>(cmin), band_min - p0)));
-        const size_t row = (static_cast<size_t>(b) * a.NKV + kvh) * a.capacity + static_cast<size_t>(p0);
-        prefetch_l2((is_k ? a.k : a.v) + row * HS, static_cast<uint32_t>(nmin) * HS * 2);
-      }
-    }
-  }
+  if (warp == W_COPY && lane < 2 * NMAP) prefetch_tensor_map(lane < NMAP ? &maps.k[lane] : &maps.v[lane - NMAP]);
   __syncthreads();
   grid_dependency_wait();
   grid_launch_dependents();
@@ -320,7 +306,7 @@ __global__ void __launch_bounds__(um::THREADS, 1)
   bool failed = false;
 
   // The MMA warp allocates the tensor memory; it and the softmax warps meet
-  // before using it. The copy warps need none and start at once.
+  // before using it. The copy warp needs none and starts at once.
   uint32_t tmem = 0;
   if (warp >= W_MMA) {
     if (warp == W_MMA) {
@@ -333,29 +319,43 @@ __global__ void __launch_bounds__(um::THREADS, 1)
     tmem = *reinterpret_cast<const uint32_t*>(smem + OFF_TMEM);
   }
 
-  if (warp == W_K || warp == W_V) {
-    // ---------------------------------------------------------- copy warps
-    const bool is_k = warp == W_K;
-    const CUtensorMap* mp = is_k ? maps.k : maps.v;
-    const uint16_t* src = is_k ? a.k : a.v;
-    const int nring = is_k ? NK : NVP;
-    const int per = is_k ? 1 : 2;  // chunks per ring slot
-    const uint32_t ring = base + (is_k ? OFF_K : OFF_V);
-    const uint32_t slot_bytes = per * CHUNK_BYTES;
-    const uint32_t fullb = is_k ? full_k : full_v, emptyb = is_k ? empty_k : empty_v;
+  if (warp == W_COPY) {
+    // ------------------------------------------------------------ copy warp
+    // One stream of 32 KB pairs (128 positions x 128 dims) through one ring:
+    // K(0), then V(i) and K(i + 1) alternately, then the last tile's V. V(i)
+    // is requested while K(i + 1) streams, so it lands about when P(i) is
+    // ready instead of holding slots through the softmax, and the scores of
+    // tile i + 1 never wait for V.
     uint32_t st_issued = 0, st_par = 0;
-    int seq = 0;
-    for (int t = 0; t < ntiles; ++t) {
+    const int total = 2 * NPAIR * ntiles;
+    // The rows of the slice's last tile that do not fill 8 (its only partial
+    // tile) come from the lanes: all of a tensor's pieces of that tile are
+    // loaded at its first pair, in one round trip, and stored pair by pair.
+    // K of the last tile is done before its V starts, so one array serves.
+    uint4 tailv[MAX_TAIL];
+    for (int e = 0; e < total; ++e) {
+      bool is_k;
+      int t, pr;
+      if (e < NPAIR) {
+        is_k = true, t = 0, pr = e;
+      } else {
+        const int m = e - NPAIR, i = m / (2 * NPAIR), r = m % (2 * NPAIR);
+        if (i + 1 < ntiles) {
+          is_k = r & 1, pr = r >> 1, t = is_k ? i + 1 : i;
+        } else {
+          is_k = false, pr = r, t = i;
+        }
+      }
+      const CUtensorMap* mp = is_k ? maps.k : maps.v;
+      const uint16_t* src = is_k ? a.k : a.v;
       const int nv = min(T, n - t * T);
       const int nv8 = nv & ~7;      // rows the TMA boxes bring
       const int nrem = nv - nv8;    // the slice's last rows: loaded by the lanes
       const int y0 = row0 + t * T;  // cache row of the tile's first position
-      // the tail rows of every chunk of this tile, all loads in flight at once
-      uint4 tailv[MAX_TAIL];
-      if (nrem > 0) {
+      if (nrem > 0 && pr == 0) {
 #pragma unroll
-        for (int k = 0; k < MAX_TAIL; ++k) {
-          const int i = lane + 32 * k;  // piece i: chunk i / (8 nrem), row nv8 + (i / 8) % nrem, piece i % 8
+        for (int k = 0; k < MAX_TAIL; ++k) {  // piece i: chunk i / (8 nrem), row nv8 + (i / 8) % nrem, piece i % 8
+          const int i = lane + 32 * k;
           tailv[k] = make_uint4(0, 0, 0, 0);
           if (i < NCH * nrem * 8) {
             const int c = i / (nrem * 8), rr = nv8 + (i / 8) % nrem, j = i % 8;
@@ -363,75 +363,74 @@ __global__ void __launch_bounds__(um::THREADS, 1)
           }
         }
       }
-      for (int u = 0; u < NCH / per; ++u, ++seq) {
-        const int slot = seq % nring, use = seq / nring;
-        if (use > 0) mbar_wait(emptyb + 8 * slot, (use - 1) & 1, failed);
-        const uint32_t dst = ring + slot * slot_bytes;
-        const uint32_t fb = fullb + 8 * slot;
-        unsigned char* dsts = smem + (dst - base);
-        if (!is_k && nv < T) {
-          // V rows past the tile's valid positions: zero, so their 0 weights
-          // add exactly 0 (stale shared memory may hold any bit pattern)
-          const int words = (T - nv) * (DC * 2 / 16);  // 16-byte words per chunk
-          for (int w = lane; w < 2 * words; w += 32) {
-            const int ch = w / words, rem = w % words;
-            *reinterpret_cast<uint4*>(dsts + ch * CHUNK_BYTES + (nv + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        if (lane == 0) {
-          mbar_expect_tx(fb, static_cast<uint32_t>(per * nv8) * 128);
-          for (int h = 0; h < per; ++h) {
-            const int c = u * per + h;
-            const uint32_t d = dst + h * CHUNK_BYTES;
-            if (nv8 == T) {
-              tma_load_2d(d, &mp[0], c * DC, y0, fb);
-            } else {
-              int r = 0;
+      const int slot = e % NPS, use = e / NPS;
+      if (use > 0) mbar_wait(empty + 8 * slot, (use - 1) & 1, failed);
+      const uint32_t dst = base + OFF_RING + slot * PAIR_BYTES;
+      const uint32_t fb = full + 8 * slot;
+      unsigned char* dsts = smem + (dst - base);
+      if (lane == 0) {
+        mbar_expect_tx(fb, static_cast<uint32_t>(2 * nv8) * 128);
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * pr + h;
+          const uint32_t d = dst + h * CHUNK_BYTES;
+          if (nv8 == T) {
+            tma_load_2d(d, &mp[0], c * DC, y0, fb);
+          } else {
+            int r = 0;
 #pragma unroll
-              for (int bi = 1; bi < NMAP; ++bi) {
-                const int bh = T >> bi;
-                if (nv8 & bh) {
-                  tma_load_2d(d + r * 128, &mp[bi], c * DC, y0 + r, fb);
-                  r += bh;
-                }
+            for (int bi = 1; bi < NMAP; ++bi) {
+              const int bh = T >> bi;
+              if (nv8 & bh) {
+                tma_load_2d(d + r * 128, &mp[bi], c * DC, y0 + r, fb);
+                r += bh;
               }
             }
           }
         }
-        if (nrem > 0) {
-          // rows [nv8, nv) of this slot's chunks: 16-byte pieces into the
-          // 128-byte swizzle (piece j of row r sits at 16 * (j ^ (r % 8)))
+      }
+      const int nz = ((nv + 15) & ~15) - nv;  // V rows the last 16-row P.V step reads past the tile
+      if (!is_k && nz > 0) {
+        // zero them, so their 0 weights add exactly 0 (stale shared memory may
+        // hold any bit pattern). P.V reads no row past that step, and with
+        // 16-position chunks only a split ending at the band's end has any.
+        const int words = nz * (DC * 2 / 16);  // 16-byte words per chunk
+        for (int w = lane; w < 2 * words; w += 32) {
+          const int ch = w / words, rem = w % words;
+          *reinterpret_cast<uint4*>(dsts + ch * CHUNK_BYTES + (nv + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (nrem > 0) {
+        // this pair's pieces, into the 128-byte swizzle (piece j of row r
+        // sits at 16 * (j ^ (r % 8)))
 #pragma unroll
-          for (int k = 0; k < MAX_TAIL; ++k) {
-            const int i = lane + 32 * k;
-            const int c = i / (nrem * 8);
-            if (i < NCH * nrem * 8 && c >= u * per && c < u * per + per) {
-              const int rr = nv8 + (i / 8) % nrem, j = i % 8;
-              *reinterpret_cast<uint4*>(dsts + (c - u * per) * CHUNK_BYTES + rr * 128 + ((j ^ (rr & 7)) << 4)) =
-                  tailv[k];
-            }
+        for (int k = 0; k < MAX_TAIL; ++k) {
+          const int i = lane + 32 * k;
+          const int c = i / (nrem * 8);
+          if (i < NCH * nrem * 8 && (c >> 1) == pr) {
+            const int rr = nv8 + (i / 8) % nrem, j = i % 8;
+            *reinterpret_cast<uint4*>(dsts + (c & 1) * CHUNK_BYTES + rr * 128 + ((j ^ (rr & 7)) << 4)) = tailv[k];
           }
         }
-        if (nrem > 0 || (!is_k && nv < T)) fence_proxy_async_smem();  // lanes' stores -> the tensor cores' view
-        __syncwarp();
-        if (lane == 0) mbar_arrive(fb);
-        st_issued |= 1u << slot;
-        st_par = (st_par & ~(1u << slot)) | (static_cast<uint32_t>(use & 1) << slot);
       }
+      if (nrem > 0 || (!is_k && nz > 0)) fence_proxy_async_smem();  // lanes' stores -> the tensor cores' view
+      __syncwarp();
+      if (lane == 0) mbar_arrive(fb);
+      st_issued |= 1u << slot;
+      st_par = (st_par & ~(1u << slot)) | (static_cast<uint32_t>(use & 1) << slot);
     }
     // No copy of this block may still be in flight when it leaves: wait for
     // the last phase issued into each slot (bounded, own failure flag).
     bool dfail = false;
-    for (int k = 0; k < nring; ++k)
-      if ((st_issued >> k) & 1u) mbar_wait(fullb + 8 * k, (st_par >> k) & 1u, dfail);
+    for (int k = 0; k < NPS; ++k)
+      if ((st_issued >> k) & 1u) mbar_wait(full + 8 * k, (st_par >> k) & 1u, dfail);
   } else if (warp == W_MMA) {
     // ----------------------------------------------------- MMA issue thread
     if (lane == 0) {
       mbar_wait(q_ready, 0, failed);
       tc_fence_after();
-      int kt = 0, kc = 0, kseq = 0;  // next score MMAs: tile kt, chunk kc; K ring sequence
-      int vt = 0, vp = 0, vseq = 0;  // next P.V MMAs: tile vt, dims block vp; V ring sequence
+      int kt = 0, kp = 0;  // next score MMAs: tile kt, K pair kp
+      int vt = 0, vp = 0;  // next P.V MMAs: tile vt, V pair (128-dim block) vp
       bool s_ok = false, p_ok = false;
       uint64_t t_idle = 0;
       uint32_t spins = 0;  // polls without progress; the clock is read every 4096
@@ -440,20 +439,23 @@ __global__ void __launch_bounds__(um::THREADS, 1)
         if (kt < ntiles) {
           // S buffer kt % 2 is free once the softmax has read S(kt - 2)
           if (!s_ok) s_ok = kt < 2 || mbar_test(s_free + 8 * (kt & 1), ((kt - 2) >> 1) & 1);
-          const int slot = kseq % NK;
-          if (s_ok && mbar_test(full_k + 8 * slot, (kseq / NK) & 1)) {
+          const int e = seq_k(kt, kp), slot = e % NPS;
+          if (s_ok && mbar_test(full + 8 * slot, (e / NPS) & 1)) {
             tc_fence_after();
-            const uint32_t kb = base + OFF_K + slot * CHUNK_BYTES;
-            const uint32_t qb = base + OFF_Q + kc * ATOM_Q;
+            const uint32_t kb = base + OFF_RING + slot * PAIR_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < DC / 16; ++kk)
-              umma_bf16(tmem + 16 * (kt & 1), sw128_desc(kb + 32 * kk, 16, 1024), sw128_desc(qb + 32 * kk, 16, 1024),
-                        kIdescQK, (kc | kk) != 0);
-            umma_commit(empty_k + 8 * slot);
-            ++kseq;
-            if (++kc == NCH) {
+            for (int h = 0; h < 2; ++h) {
+              const int c = 2 * kp + h;
+              const uint32_t qb = base + OFF_Q + c * ATOM_Q;
+#pragma unroll
+              for (int kk = 0; kk < DC / 16; ++kk)
+                umma_bf16(tmem + 16 * (kt & 1), sw128_desc(kb + h * CHUNK_BYTES + 32 * kk, 16, 1024),
+                          sw128_desc(qb + 32 * kk, 16, 1024), kIdescQK, (c | kk) != 0);
+            }
+            umma_commit(empty + 8 * slot);
+            if (++kp == NPAIR) {
               umma_commit(s_full + 8 * (kt & 1));
-              kc = 0;
+              kp = 0;
               ++kt;
               s_ok = false;
             }
@@ -462,22 +464,21 @@ __global__ void __launch_bounds__(um::THREADS, 1)
         }
         if (vt < kt) {
           if (!p_ok) p_ok = mbar_test(p_ready + 8 * (vt & 1), (vt >> 1) & 1);
-          const int slot = vseq % NVP;
-          if (p_ok && mbar_test(full_v + 8 * slot, (vseq / NVP) & 1)) {
+          const int e = seq_v(vt, vp, ntiles), slot = e % NPS;
+          if (p_ok && mbar_test(full + 8 * slot, (e / NPS) & 1)) {
             tc_fence_after();
-            const uint32_t vb = base + OFF_V + slot * PAIR_BYTES;
+            const uint32_t vb = base + OFF_RING + slot * PAIR_BYTES;
             const uint32_t pb = base + OFF_P + (vt & 1) * P_BUF;
             const uint32_t d = tmem + 32 + 16 * vp;
-#pragma unroll
-            for (int kk = 0; kk < T / 16; ++kk) {
+            const int nk = (min(T, n - vt * T) + 15) >> 4;  // 16-position steps holding valid rows
+            for (int kk = 0; kk < nk; ++kk) {
               const uint64_t adesc = sw128_desc(vb + kk * 2048, CHUNK_BYTES, 1024);
               const uint32_t patom = pb + (kk >> 2) * ATOM_Q + (kk & 3) * 32;
               umma_bf16(d, adesc, sw128_desc(patom, 16, 1024), kIdescPV, (vt > 0 || kk > 0) ? 1u : 0u);
               umma_bf16(d, adesc, sw128_desc(patom + P_HALF, 16, 1024), kIdescPV, 1u);
             }
-            umma_commit(empty_v + 8 * slot);
-            ++vseq;
-            if (++vp == NCH / 2) {
+            umma_commit(empty + 8 * slot);
+            if (++vp == NPAIR) {
               umma_commit(pv_done + 8 * (vt & 1));
               vp = 0;
               ++vt;

@@ -149,16 +149,16 @@ enum {
  * Tensor-memory kernel (opt-in through fd_plan_override(..., FD_PATH_UMMA, ...);
  * plans never choose it): for the MQA geometry of "One KV head breaks the
  * textbook" (bf16, HS 512, 8 < G <= 16, window <= 0) each split block takes a
- * consecutive slice of the band's slots [0, min(len, capacity)), streams K and
- * V through two separate shared-memory rings as TMA boxes of 128/64/32/16/8
- * rows (the last rows of a slice that do not fill 8 are loaded by the copy
- * warp, so exactly the band is read), and one thread issues S^T = K Q^T and
- * O^T += V^T P^T as tcgen05 MMAs with the accumulators in tensor memory,
- * the next tile's scores while the current tile's softmax runs. Such a plan
- * has group_bytes = 16384 (one TMA box), consumer_warps = 4, cluster = 1 and
- * no fused merge; the merge kernel is the same. Measured slower than
- * FD_PATH_TC on GB300 (a 128-position tile of K and V is larger than shared
- * memory, so each block streams at about 60% of its share of HBM).
+ * consecutive slice of the band's slots [0, min(len, capacity)) in chunks of
+ * 16 positions (granule 16), streams K and V through one shared-memory ring
+ * of 32 KB slots as TMA boxes of 128/64/32/16/8 rows in the order K(0), then
+ * V(i) and K(i + 1) alternately (the last rows of the band that do not fill 8
+ * are loaded by the copy warp, so exactly the band is read), and one thread
+ * issues S^T = K Q^T and O^T += V^T P^T as tcgen05 MMAs with the accumulators
+ * in tensor memory, the next tile's scores while the current tile's softmax
+ * runs. Such a plan has group_bytes = 16384 (one TMA box), consumer_warps = 4,
+ * cluster = 1 and no fused merge; the merge kernel is the same. Measured on
+ * GB300: level with FD_PATH_TC on long MQA bands, slower on short ones.
  *
  * Clusters (opt-in through fd_plan_override; plans use cluster = 1): the
  * blocks of `cluster` consecutive splits form a thread-block cluster and
@@ -171,7 +171,7 @@ typedef struct {
   int num_splits;          /* S: grid splits per (sequence, KV head) */
   int path;                /* FD_PATH_SIMT, FD_PATH_TC or FD_PATH_UMMA */
   int cluster;             /* blocks per cluster along the splits; divides S; 1 = none */
-  int granule;             /* chunk rounding on the device, positions: 1, or the tile for short bands */
+  int granule;             /* chunk rounding on the device, positions: 1, or the tile for short bands; 16 for FD_PATH_UMMA */
   int max_band;            /* band bound the plan was sized for */
   int ctas_per_sm;         /* resident CTAs per SM the plan assumed */
   int num_sms;             /* SM count the plan assumed */

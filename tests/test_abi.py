@@ -290,6 +290,7 @@ def test_tcgen05_family_is_opt_in_and_shape_bound(lib):
     p = _plan(WORKLOADS["gemma_global_mqa_32k"])
     fd.fd_plan_override(p, 0, fd.FD_PATH_UMMA)
     assert p.path == fd.FD_PATH_UMMA and p.group_bytes == 16384 and p.consumer_warps == 4
+    assert p.granule == 16  # only the band's last split can end off a 16-row P.V step
     for w in (WORKLOADS["gemma_local_ring"], WORKLOADS["llama_tiny"]):
         q = _plan(w)
         with pytest.raises(fd.FdError):
