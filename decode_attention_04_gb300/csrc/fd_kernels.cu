@@ -274,7 +274,7 @@ struct TcCfg {
   static constexpr size_t SMEM = OFF_BAR + 2 * NSTAGE * 8;
   // blocks per SM the shared memory allows (two when a block takes at most
   // half of the SM's 228 KB, less the 1 KB the driver reserves per block);
-  // the fused-merge instance is held to it by a register bound (the plain
+  // the in-launch merge instances are held to it by a register bound (the plain
   // instance is left to the compiler, which keeps it leaner)
   static constexpr int MINB = SMEM + 1024 <= 114 * 1024 ? 2 : 1;
   // Register budget of the plain per-split instance (0: the compiler's
@@ -287,8 +287,9 @@ struct TcCfg {
   // so only these configurations take one. Where one-tile splits wait for the
   // merge kernel, that kernel's blocks must fit beside two split blocks (the
   // ring tile at 82 registers, where none fits, 7.0; the compiler's choice
-  // without the fused merge in the instance, 6.1). The fused-merge instance
-  // is held by its launch bounds to the occupancy its shared memory allows.
+  // without the fused merge in the instance, 6.1). The in-launch merge
+  // instances are held by their launch bounds to the occupancy their shared
+  // memory allows (the group step needs every block resident at once).
   static constexpr int MAXREG = MAXREG_;
 
   // tile position held by MMA row m, and its byte offset in a stage
@@ -603,8 +604,8 @@ __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
     // no copy may land after the block has left (tiles copied early for a
     // length below the plan's bound)
     if (!persist && warp >= C::NWC) producer_drain<C>(full0, st_issued, st_par);
-    // len == 0: the output row is zero. With one block per band, or with the
-    // fused merge (no block of an empty band ever merges), block 0 writes it.
+    // len == 0: the output row is zero. With one block per band, or with an
+    // in-launch merge (no block of an empty band ever merges), block 0 writes it.
     if (direct || (FUSED && band == 0 && s == 0)) {
       for (int i = tid; i < G * C::HS; i += C::THREADS) {
         const size_t o = (static_cast<size_t>(b) * a.NH + hbase + i / C::HS) * C::HS + i % C::HS;
@@ -1857,7 +1858,7 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
     e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, a, stream);
   }
   // the split kernel wrote the output itself: one block / cluster per band, or
-  // the fused merge by each group's last block
+  // an in-launch merge (each group's last block, or the group step)
   if (e != cudaSuccess || a.num_splits == a.cluster || a.fused) return e;
   if (static_cast<long long>(a.B) * a.NH < kMergeStagedRows) {
     // one round trip of loads per warp: 8 slots each up to 64 partials per
