@@ -148,6 +148,23 @@ def test_group_step_merge_matches_oracle_and_merge_kernel(w):
         fd.fd_plan_override(fd.fd_plan_t.from_buffer_copy(plan), s_cap + 1, 0, 1, 2)
 
 
+def test_group_step_with_min_len_bound():
+    """The group step behind early reads: with the plan's lower bound on the
+    lengths kept, the result equals the plan without it; broken, it is still
+    exact and FD_DEVERR_MIN_LEN is raised; the counter words are zero after
+    both."""
+    w = W("gs_min_len", 1, 16, 8, 256, 1024, 1024, lens=(700,), seed=79)
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    base = run(w, q, k, v, lens, splits=32, cluster=1, fused=2)
+    kept = run(w, q, k, v, lens, splits=32, cluster=1, fused=2, min_len=700)
+    check(kept, ref, what="group step, min_len kept")
+    assert kept["deverr"] == 0 and torch.equal(kept["out32"], base["out32"])
+    broken = run(w, q, k, v, lens, splits=32, cluster=1, fused=2, min_len=1024)
+    check(broken, ref, what="group step, min_len broken")
+    assert broken["deverr"] & fd.FD_DEVERR_MIN_LEN
+
+
 def test_group_step_graph_replays_reuse_the_counters():
     """A captured group-step call replayed with new lengths: every replay is
     exact (the counter words return to zero each time), and the E4M3 cache

@@ -162,3 +162,39 @@ def test_umma_nan_key_in_a_middle_tile_reaches_every_row():
     assert torch.isnan(res["out32"][0]).all()
     res = _umma_run(w, q, k, v, lens, splits=4)
     assert torch.isnan(res["out32"][0]).all()
+
+
+@pytest.mark.parametrize("splits", [1, 5, 40])
+def test_umma_min_len_bound_kept_and_broken(splits):
+    """The tcgen05 kernel reads nothing before a sequence's length arrives, so
+    the plan's lower bound on the lengths changes no result: kept, the output
+    is bit-identical to the plan without it and no error bit is set; broken,
+    the output is still exact and FD_DEVERR_MIN_LEN is raised."""
+    w = Workload("u_min_len", 2, 16, 1, 512, 2048, 0, lens=(1500, 700), seed=72)
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    base = _umma_run(w, q, k, v, lens, splits=splits)
+    kept = _umma_run(w, q, k, v, lens, splits=splits, min_len=700)
+    check(kept, ref, what=f"umma min_len kept S={splits}")
+    assert kept["deverr"] == 0
+    assert torch.equal(kept["out32"], base["out32"])
+    broken = _umma_run(w, q, k, v, lens, splits=splits, min_len=1024)
+    check(broken, ref, what=f"umma min_len broken S={splits}")
+    assert broken["deverr"] & fd.FD_DEVERR_MIN_LEN
+
+
+def test_umma_chunks_are_whole_16_position_steps():
+    """Plans for the tcgen05 kernel round chunks to 16 positions: every split
+    but the band's last ends on a P.V step, and results do not depend on the
+    split count even where a chunk of 1 position would have been asked for."""
+    w = Workload("u_granule", 1, 16, 1, 512, 4096, 0, lens=(1000,), seed=73)
+    q, k, v, lens = make_inputs(w)
+    ref = oracle_ref(w, q, k, v, lens)
+    outs = []
+    for splits in (7, 63, 152, 1000):
+        res = _umma_run(w, q, k, v, lens, splits=splits)
+        assert res["plan"].granule == 16
+        check(res, ref, what=f"umma granule S={splits}")
+        outs.append(res["out32"])
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 2e-3
