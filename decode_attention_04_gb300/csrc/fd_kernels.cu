@@ -1689,8 +1689,13 @@ using Tc128x2 = TcCfg<128, 2, 4, 3>;
 using Tc256x1 = TcCfg<256, 1, 8, 3>;
 using Tc256x2 = TcCfg<256, 2, 8, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;  // a 16-position tile has 8 x 16 softmax slots
-using Tc512x2 = TcCfg<512, 2, 8, 3, 2048, false, 96>;      // two blocks per SM (long MQA bands)
-using Tc512x2w = TcCfg<512, 2, 8, 3, 4096, false, 96>;  // one block per SM, 4 KB copies
+// The head-dim-512 bf16 tiles stream through two stages, not three (measured
+// on GB300, us per layer: MQA 32k 19.25 -> 18.9, MQA 4k 8.83 -> 8.63 on the
+// one-block-per-SM tile; MQA long 166.0 -> 163.8 on the two-blocks-per-SM
+// tile): the copies of one stage cover a tile's math, and the smaller block
+// leaves the SM more L1.
+using Tc512x2 = TcCfg<512, 2, 8, 2, 2048, false, 96>;      // two blocks per SM (long MQA bands)
+using Tc512x2w = TcCfg<512, 2, 8, 2, 4096, false, 96>;  // one block per SM, 4 KB copies
 // E4M3 caches: a block's copy rate is set by the number of bulk copies it
 // issues, so 2 KB E4M3 groups (the positions of a 4 KB bf16 group) in a
 // two-stage ring, except head dim 256 (small sliding bands), where 1 KB groups
