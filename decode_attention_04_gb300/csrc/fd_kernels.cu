@@ -1686,7 +1686,12 @@ using Tc64x1 = TcCfg<64, 1, 4, 3>;
 using Tc64x2 = TcCfg<64, 2, 4, 3>;
 using Tc128x1 = TcCfg<128, 1, 4, 3>;
 using Tc128x2 = TcCfg<128, 2, 4, 3>;
-using Tc256x1 = TcCfg<256, 1, 8, 3>;
+// The head-dim-256 tile for up to 8 query rows (the sliding ring) copies 4 KB
+// groups (64-position tiles, one block per SM) through two stages: the ring's
+// band becomes 16 one-tile splits per KV head instead of 32 of 32 positions
+// (measured on GB300, us per layer: 6.14 with 2 KB groups in three stages,
+// 6.04 with 4 KB groups in three, 5.99 in two).
+using Tc256x1 = TcCfg<256, 1, 8, 2, 4096>;
 using Tc256x2 = TcCfg<256, 2, 8, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;  // a 16-position tile has 8 x 16 softmax slots
 // The head-dim-512 bf16 tiles stream through two stages, not three (measured

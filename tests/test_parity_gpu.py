@@ -156,11 +156,13 @@ def test_group_step_with_min_len_bound():
     w = W("gs_min_len", 1, 16, 8, 256, 1024, 1024, lens=(700,), seed=79)
     q, k, v, lens = make_inputs(w)
     ref = oracle_ref(w, q, k, v, lens)
-    base = run(w, q, k, v, lens, splits=32, cluster=1, fused=2)
-    kept = run(w, q, k, v, lens, splits=32, cluster=1, fused=2, min_len=700)
+    plan = fd.fd_plan(w.B, w.NH, w.NKV, w.HS, w.capacity, w.window)
+    S = min(16, plan.num_sms * plan.ctas_per_sm // (w.B * w.NKV))  # one wave
+    base = run(w, q, k, v, lens, splits=S, cluster=1, fused=2)
+    kept = run(w, q, k, v, lens, splits=S, cluster=1, fused=2, min_len=700)
     check(kept, ref, what="group step, min_len kept")
     assert kept["deverr"] == 0 and torch.equal(kept["out32"], base["out32"])
-    broken = run(w, q, k, v, lens, splits=32, cluster=1, fused=2, min_len=1024)
+    broken = run(w, q, k, v, lens, splits=S, cluster=1, fused=2, min_len=1024)
     check(broken, ref, what="group step, min_len broken")
     assert broken["deverr"] & fd.FD_DEVERR_MIN_LEN
 
