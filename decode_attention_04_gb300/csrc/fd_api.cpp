@@ -138,6 +138,7 @@ int group_rule(const fd_plan_t& p) {
     const int short_tile = fd::tc_short_tile_positions(p.HS);
     return (p.HS == 256 || (short_tile > 0 && p.granule == short_tile)) ? 1024 : 2048;
   }
+  if (p.path == FD_PATH_TC && p.HS == 256 && G <= 8) return 4096;  // the sliding ring's tile
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;
 }
 
@@ -433,6 +434,10 @@ int run(const fd_plan_t& plan, void* workspace, size_t workspace_bytes, float* o
   a.path = plan.path;
   a.min_len = plan.min_len;
   a.withhold_tile = g_withhold_tile.load(std::memory_order_relaxed);
+  // whole-tile splits that cover the plan's band bound: one tile per block (a
+  // longer band than the bound stays exact, its blocks just take two tiles)
+  a.one_tile = plan.path == FD_PATH_TC && plan.persistent == 0 && plan.granule > 1 &&
+               static_cast<long long>(plan.max_band) <= static_cast<long long>(plan.num_splits) * plan.granule;
   a.scale_log2 = scale * 1.4426950408889634f;
   return fd::launch_decode(a, stream) == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }

@@ -44,6 +44,8 @@ struct LaunchArgs {
                             // [0, min(min_len, capacity)) are live before the lengths are read
   int withhold_tile;        // test hook: tensor-core split blocks issue no copies from this tile of
                             // theirs on (a huge value: off)
+  int one_tile;             // 1: the plan gives every split at most one tile (whole-tile splits
+                            // covering its band bound), so a one-stage tile may serve it
   float scale_log2;         // scale * log2(e)
 };
 

@@ -1241,6 +1241,11 @@ __device__ __forceinline__ void split_tc_body(const LaunchArgs& a) {
   // a cluster barrier, block `rank` combines head dims
   // [rank * HS / CS, (rank + 1) * HS / CS) of every row over the CS blocks:
   // M = max_c m_c, w_c = 2^(m_c - M), O = sum_c w_c O_c, L = sum_c w_c l_c.
+  // A block whose slice turned out empty (a length below the plan's bound)
+  // may still have its first tile's early copies in flight into stage 0: they
+  // must land before O is parked over that stage. A block with tiles waited
+  // for every copy it issued when it consumed them.
+  if (n_early > 0 && ntiles == 0 && warp < C::NWC) mbar_wait(full0, 0, failed);
   float* sO = reinterpret_cast<float*>(smem + C::OFF_K);
   if (warp < C::NWC) {
 #pragma unroll
@@ -1687,11 +1692,14 @@ using Tc64x2 = TcCfg<64, 2, 4, 3>;
 using Tc128x1 = TcCfg<128, 1, 4, 3>;
 using Tc128x2 = TcCfg<128, 2, 4, 3>;
 // The head-dim-256 tile for up to 8 query rows (the sliding ring) copies 4 KB
-// groups (64-position tiles, one block per SM) through two stages: the ring's
-// band becomes 16 one-tile splits per KV head instead of 32 of 32 positions
-// (measured on GB300, us per layer: 6.14 with 2 KB groups in three stages,
-// 6.04 with 4 KB groups in three, 5.99 in two).
+// groups (64-position tiles) through two stages: the ring's band becomes 16
+// one-tile splits per KV head instead of 32 of 32 positions (measured on
+// GB300, us per layer: 6.14 with 2 KB groups in three stages, 6.04 with 4 KB
+// groups in three, 5.99 in two). When the plan gives every split at most one
+// tile, a one-stage instance serves it (half the shared memory, 5.84 against
+// 6.04 on the same box); a split with more tiles would wait for each copy.
 using Tc256x1 = TcCfg<256, 1, 8, 2, 4096>;
+using Tc256x1s = TcCfg<256, 1, 8, 1, 4096>;
 using Tc256x2 = TcCfg<256, 2, 8, 3>;
 using Tc512x1 = TcCfg<512, 1, 4, 3>;  // a 16-position tile has 8 x 16 softmax slots
 // The head-dim-512 bf16 tiles stream through two stages, not three (measured
@@ -1725,7 +1733,7 @@ using Tc128x1fs = TcCfg<128, 1, 4, 4, 2048, true>;
 using Tc128x2fs = TcCfg<128, 2, 4, 4, 2048, true>;
 
 template <template <class> class Fn, class... Args>
-cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, int warps, Args&&... args) {
+cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, int warps, bool one_tile, Args&&... args) {
   const bool two = G > 8;
   if (kv8) {
     switch (HS) {
@@ -1745,7 +1753,9 @@ cudaError_t with_tc_cfg(int HS, int G, int group_bytes, bool kv8, int warps, Arg
   switch (HS) {
     case 64: return two ? Fn<Tc64x2>::run(args...) : Fn<Tc64x1>::run(args...);
     case 128: return two ? Fn<Tc128x2>::run(args...) : Fn<Tc128x1>::run(args...);
-    case 256: return two ? Fn<Tc256x2>::run(args...) : Fn<Tc256x1>::run(args...);
+    case 256:
+      if (two) return Fn<Tc256x2>::run(args...);
+      return one_tile ? Fn<Tc256x1s>::run(args...) : Fn<Tc256x1>::run(args...);
     case 512:
       if (!two) return Fn<Tc512x1>::run(args...);
       return group_bytes >= 4096 ? Fn<Tc512x2w>::run(args...) : Fn<Tc512x2>::run(args...);
@@ -1840,11 +1850,11 @@ cudaError_t query_ctas_per_sm(int path, int HS, int G, bool kv8, int* ctas) {
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, split_simt_kernel, kSimtThreads, sm);
   }
-  return with_tc_cfg<OccFn>(HS, G, 2048, kv8, 0, ctas);
+  return with_tc_cfg<OccFn>(HS, G, 2048, kv8, 0, false, ctas);
 }
 
 cudaError_t query_max_cluster(int HS, int G, bool kv8, int* cluster) {
-  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, 0, cluster);
+  return with_tc_cfg<MaxClusterFn>(HS, G, 2048, kv8, 0, false, cluster);
 }
 
 cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
@@ -1853,7 +1863,7 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
   LaunchArgs a = args;
   a.tile_stride = 0;
   if (a.path == FD_PATH_TC && (a.window <= 0 || a.window >= a.capacity)) {
-    e = with_tc_cfg<TileFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, &a.tile_stride);
+    e = with_tc_cfg<TileFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, a.one_tile != 0, &a.tile_stride);
     if (e != cudaSuccess) return e;
   }
   if (a.path == FD_PATH_SIMT) {
@@ -1865,7 +1875,7 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
   } else if (a.path == FD_PATH_UMMA) {
     e = launch_umma(a, stream);
   } else {
-    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, a, stream);
+    e = with_tc_cfg<LaunchFn>(a.HS, G, a.group_bytes, a.kv8 != 0, a.consumer_warps, a.one_tile != 0, a, stream);
   }
   // the split kernel wrote the output itself: one block / cluster per band, or
   // an in-launch merge (each group's last block, or the group step)

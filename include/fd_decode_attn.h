@@ -141,10 +141,12 @@ enum {
  *   sets both back to zero.
  *
  * Copy groups: a tile's K and V rows arrive in groups of about 2 KB, one
- * bulk copy per group. For head dim 512 with more than 8 query rows per KV
- * head, when the whole grid fits one wave at one block per SM, the plan uses
- * 4 KB groups (a tile that needs the whole SM's shared memory): fewer copies
- * per block, and a block's copy rate is set by its copy count.
+ * bulk copy per group. Head dim 256 with at most 8 query rows per KV head
+ * (the sliding ring) uses 4 KB groups (64-position tiles; one pipeline stage
+ * when every split of the plan is at most one tile, else two). For head dim
+ * 512 with more than 8 query rows per KV head, when the whole grid fits one
+ * wave at one block per SM, the plan uses 4 KB groups too: fewer copies per
+ * block, and a block's copy rate is set by its copy count.
  *
  * Tensor-memory kernel (opt-in through fd_plan_override(..., FD_PATH_UMMA, ...);
  * plans never choose it): for the MQA geometry of "One KV head breaks the
