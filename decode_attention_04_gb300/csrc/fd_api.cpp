@@ -133,10 +133,10 @@ int group_rule(const fd_plan_t& p) {
   const long long blocks = static_cast<long long>(p.B) * p.NKV * p.num_splits;
   if (p.path == FD_PATH_UMMA) return 16384;  // one TMA box: 128 positions x 64 dims
   if (p.kv_dtype == FD_KV_E4M3) {
-    // 1 KB groups for head dim 256, and for 64 / 128 when the plan cut the
-    // band into whole short tiles
+    // 1 KB groups for head dim 256 with more than 8 query rows, and for 64 /
+    // 128 when the plan cut the band into whole short tiles
     const int short_tile = fd::tc_short_tile_positions(p.HS);
-    return (p.HS == 256 || (short_tile > 0 && p.granule == short_tile)) ? 1024 : 2048;
+    return ((p.HS == 256 && G > 8) || (short_tile > 0 && p.granule == short_tile)) ? 1024 : 2048;
   }
   if (p.path == FD_PATH_TC && p.HS == 256 && G <= 8) return 4096;  // the sliding ring's tile
   return (p.path == FD_PATH_TC && p.HS == 512 && G > 8 && blocks <= p.num_sms) ? 4096 : 2048;

@@ -1719,7 +1719,10 @@ using Tc64x1f = TcCfg<64, 1, 2, 2, 4096, true>;  // two consumer warps: 32 dims 
 using Tc64x2f = TcCfg<64, 2, 2, 2, 4096, true>;
 using Tc128x1f = TcCfg<128, 1, 4, 2, 4096, true>;
 using Tc128x2f = TcCfg<128, 2, 4, 2, 4096, true>;
-using Tc256x1f = TcCfg<256, 1, 8, 4, 2048, true>;
+// The E4M3 ring tile: 2 KB E4M3 groups (64 positions) in two stages, like
+// the bf16 one (measured on GB300, E4M3 ring 6.66 -> 6.35-6.39 us per layer
+// against 1 KB groups in four stages).
+using Tc256x1f = TcCfg<256, 1, 8, 2, 4096, true>;
 using Tc256x2f = TcCfg<256, 2, 8, 4, 2048, true>;
 using Tc512x1f = TcCfg<512, 1, 4, 2, 4096, true>;
 using Tc512x2f = TcCfg<512, 2, 4, 2, 4096, true>;

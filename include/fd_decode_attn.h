@@ -214,7 +214,8 @@ int fd_plan_sms(int B, int NH, int NKV, int HS, int capacity, int window, int ma
  * type kv_dtype (FD_KV_BF16 gives the same plan as fd_plan / fd_plan_sms).
  * An E4M3 plan runs on FD_PATH_TC only and bounds a split by the same ~2 MiB
  * of K+V bytes, so its splits may hold twice the positions. Its copy groups
- * are 2 KB (1 KB for head dim 256) and its head-dim-512, 16-row tile uses
+ * are 2 KB (1 KB for head dim 256 with more than 8 query rows, and for the
+ * half-length tiles above) and its head-dim-512, 16-row tile uses
  * eight consumer warps when the grid is one block per SM, four otherwise
  * (measured on GB300: copy count per block and issue slots per SM).
  * Errors: FD_ERR_INVALID_ARG (unknown kv_dtype), those of fd_plan / fd_plan_sms.

@@ -198,10 +198,11 @@ def test_e4m3_plan_matches_bf16_rule_with_half_the_bytes(name, lib):
     w = WORKLOADS[name]
     p8, p16 = _plan_kv(w), _plan(w)
     assert p8.kv_dtype == fd.FD_KV_E4M3 and p16.kv_dtype == fd.FD_KV_BF16
-    # 1 KB E4M3 groups for head dim 256, and for 64 / 128 when the band is cut
-    # into whole short tiles (the half-length tile: 64 positions at d128)
+    # 1 KB E4M3 groups for head dim 256 with more than 8 query rows, and for
+    # 64 / 128 when the band is cut into whole short tiles (the half-length
+    # tile: 64 positions at d128)
     short = w.HS in (64, 128) and p8.granule > 1
-    assert p8.group_bytes == (1024 if w.HS == 256 or short else 2048) and p8.path == fd.FD_PATH_TC
+    assert p8.group_bytes == (1024 if (w.HS == 256 and w.G > 8) or short else 2048) and p8.path == fd.FD_PATH_TC
     if short:
         assert p8.granule == {64: 128, 128: 64}[w.HS]
     # consumer warps: 8 for the E4M3 head-dim-512 MQA tile only when the grid
@@ -228,7 +229,7 @@ def test_e4m3_plan_rejects_the_simt_path_and_unknown_types(lib):
         fd.fd_plan_override(p, 0, fd.FD_PATH_SIMT)
     assert e.value.status == fd.FD_ERR_INVALID_ARG
     fd.fd_plan_override(p, 9, fd.FD_PATH_TC)  # split count and clusters still move
-    assert p.num_splits == 9 and p.group_bytes == 1024 and p.consumer_warps == 8
+    assert p.num_splits == 9 and p.group_bytes == 2048 and p.consumer_warps == 8
     # the E4M3 MQA tile follows the grid: one block per SM -> 8 warps, more -> 4
     m = _plan_kv(WORKLOADS["gemma_global_mqa_32k"])
     assert m.num_splits * m.B * m.NKV <= 152 and m.consumer_warps == 8
@@ -382,7 +383,7 @@ def test_e4m3_short_band_tile(lib):
     fd.fd_plan_override(p, 0, fd.FD_PATH_TC)  # same family: unchanged
     assert p.group_bytes == 1024
     q = _plan_kv(WORKLOADS["gemma_local_ring"])
-    assert q.group_bytes == 1024 and q.granule == 32  # head dim 256 keeps its own 1 KB tile
+    assert q.group_bytes == 2048 and q.granule == 64  # the ring's tile: 2 KB E4M3 groups, 64 positions
 
 
 def test_compiled_entries_return_the_library_status(lib):
