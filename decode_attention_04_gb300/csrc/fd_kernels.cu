@@ -1336,20 +1336,21 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXREG) split_tc_ke
 
 // ================================================================ merge kernel
 
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 8;        // warps of a few-rows merge block
+constexpr int kMergeWarpsFew = 2;     // ... when a row has at most 2 x 8 partial slots
 constexpr int kMergeBatchWide = 20;   // slots per warp per round trip when a row has 64 < S <= 160
 constexpr int kMergeStagedRows = 64;  // rows (B * NH) from which the staged merge is used
 
 // The merge for few rows (B * NH < kMergeStagedRows), where it is one short
 // step in a chain of launches. One block per (32-dim slab, query head,
-// sequence); lane = dim in the slab, warp w = partial slots w, w + 8, ...;
-// each warp issues the loads of kMergeBatch partials before using any and
-// folds them into a running (max, sum, O); the eight warp results are then
+// sequence); lane = dim in the slab, warp w of W = partial slots w, w + W,
+// ...; each warp issues the loads of kMergeBatch partials before using any and
+// folds them into a running (max, sum, O); the W warp results are then
 // combined the same way: M = max_s m_s, w_s = 2^(m_s - M),
 // out = sum_s w_s O_s / sum_s w_s l_s. The first batch of loads goes out
 // with the load of the row's length (every slot is in bounds); slots past
 // the row's active splits are masked once the length has arrived.
-template <int kMergeBatch>  // partials whose loads one warp issues together
+template <int kMergeBatch, int kMergeWarps>  // partials whose loads one warp issues together; warps
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const LaunchArgs a) {
   __shared__ float sacc[kMergeWarps][32];
   __shared__ float sl[kMergeWarps];
@@ -1891,8 +1892,14 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
     dim3 mgrid(a.HS / 32, a.NH, a.B);
     const int ns = a.num_splits / a.cluster;
     if (!a.kv8 && ns > kMergeWarps * 8 && ns <= kMergeWarps * kMergeBatchWide)
-      return launch_pdl(merge_kernel<kMergeBatchWide>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
-    return launch_pdl(merge_kernel<8>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+      return launch_pdl(merge_kernel<kMergeBatchWide, kMergeWarps>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
+    // up to 16 slots: two warps, one round trip each (measured, us per layer:
+    // ring with 16 partials 5.79 -> 5.73, Llama tiny 4.78 -> 4.67; four warps
+    // were slower on the ring, 5.99, and fewer warps lose where rows have
+    // many slots, MQA 32k 19.25 -> 23.8 at two)
+    if (ns <= kMergeWarpsFew * 8)
+      return launch_pdl(merge_kernel<8, kMergeWarpsFew>, mgrid, dim3(kMergeWarpsFew * 32), 0, stream, 1, a);
+    return launch_pdl(merge_kernel<8, kMergeWarps>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
   }
   const size_t msmem = merge_smem_bytes(a.num_splits / a.cluster);
   e = smem_attr_once<merge_staged_kernel>(static_cast<int>(merge_smem_bytes(kMergeStageMax)));
