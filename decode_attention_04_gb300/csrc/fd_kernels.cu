@@ -1337,7 +1337,7 @@ __global__ void __launch_bounds__(C::THREADS) __maxnreg__(C::MAXREG) split_tc_ke
 // ================================================================ merge kernel
 
 constexpr int kMergeWarps = 8;        // warps of a few-rows merge block
-constexpr int kMergeWarpsFew = 2;     // ... when a row has at most 2 x 8 partial slots
+constexpr int kMergeFewSlots = 16;    // a row with at most this many partial slots: one warp
 constexpr int kMergeBatchWide = 20;   // slots per warp per round trip when a row has 64 < S <= 160
 constexpr int kMergeStagedRows = 64;  // rows (B * NH) from which the staged merge is used
 
@@ -1893,12 +1893,14 @@ cudaError_t launch_decode(const LaunchArgs& args, cudaStream_t stream) {
     const int ns = a.num_splits / a.cluster;
     if (!a.kv8 && ns > kMergeWarps * 8 && ns <= kMergeWarps * kMergeBatchWide)
       return launch_pdl(merge_kernel<kMergeBatchWide, kMergeWarps>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
-    // up to 16 slots: two warps, one round trip each (measured, us per layer:
-    // ring with 16 partials 5.79 -> 5.73, Llama tiny 4.78 -> 4.67; four warps
-    // were slower on the ring, 5.99, and fewer warps lose where rows have
-    // many slots, MQA 32k 19.25 -> 23.8 at two)
-    if (ns <= kMergeWarpsFew * 8)
-      return launch_pdl(merge_kernel<8, kMergeWarpsFew>, mgrid, dim3(kMergeWarpsFew * 32), 0, stream, 1, a);
+    // up to 16 slots: one warp, every slot's loads in one round trip
+    // (measured in same-box A/Bs, us per layer: eight warps -> two, ring with
+    // 16 partials 5.79 -> 5.73, Llama tiny 4.78 -> 4.67; two -> one, ring
+    // 5.68 -> 5.58, tiny 4.70 -> 4.62; four warps were slower on the ring,
+    // 5.99, and few warps lose where rows have many slots, MQA 32k 19.25 ->
+    // 23.8 at two)
+    if (ns <= kMergeFewSlots)
+      return launch_pdl(merge_kernel<kMergeFewSlots, 1>, mgrid, dim3(32), 0, stream, 1, a);
     return launch_pdl(merge_kernel<8, kMergeWarps>, mgrid, dim3(kMergeWarps * 32), 0, stream, 1, a);
   }
   const size_t msmem = merge_smem_bytes(a.num_splits / a.cluster);
