@@ -472,3 +472,28 @@ def test_group_step_plan_rules(lib):
     rc = lib.fd_decode_attn_ex(ctypes.byref(bad), dummy, bad.workspace_bytes, None, dummy, dummy, dummy, dummy,
                                dummy, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, 0.0, None)
     assert rc == fd.FD_ERR_INVALID_ARG
+
+
+# (workload) -> (bf16 splits, granule, group bytes), (E4M3 splits, granule, group bytes)
+# on 152 SMs x 2 CTAs: the sliding ring takes 64-position tiles (4 KB bf16 / 2 KB
+# E4M3 groups) as 16 one-tile splits; B = 1 MQA the wide 4 KB tile; Llama tiny
+# whole 64-position tiles (the E4M3 half-length 1 KB tile)
+PLAN_TABLE = {
+    "llama_tiny": ((8, 64, 2048), (8, 64, 1024)),
+    "gemma_local_ring": ((16, 64, 4096), (16, 64, 2048)),
+    "gemma_global_mqa_4k": ((152, 1, 4096), (152, 1, 2048)),
+    "gemma_global_mqa_32k": ((152, 1, 4096), (152, 1, 2048)),
+    "llama_ragged": ((9, 1, 2048), (6, 1, 2048)),
+    "gemma_mqa_long": ((76, 1, 2048), (76, 1, 2048)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLAN_TABLE))
+def test_plan_table_of_the_benchmark_workloads(name, lib):
+    """The split count, chunk granule and copy-group size each benchmark
+    workload's plan takes, for both cache types."""
+    w = WORKLOADS[name]
+    p, p8 = _plan(w), _plan_kv(w)
+    want, want8 = PLAN_TABLE[name]
+    assert (p.num_splits, p.granule, p.group_bytes) == want
+    assert (p8.num_splits, p8.granule, p8.group_bytes) == want8
