@@ -206,6 +206,19 @@ def test_group_step_graph_replays_reuse_the_counters():
     assert fd.fd_get_device_error() == 0
 
 
+@pytest.mark.parametrize("hs,nh,nkv", [(256, 16, 8), (128, 32, 8), (512, 16, 1)], ids=["d256", "d128", "d512"])
+def test_lengths_beyond_the_plan_bound_stay_exact(hs, nh, nkv):
+    """A plan sized for short bands (max_len = 128: whole-tile splits, and for
+    the sliding-ring tile its one-stage form, each split one tile) called with
+    far longer bands: the device divides each band itself, so every split just
+    takes several tiles through its stages and the result stays exact."""
+    w = W(f"beyond_d{hs}", 2, nh, nkv, hs, 2048, 0, lens=(2000, 700), seed=80 + hs)
+    q, k, v, lens = make_inputs(w)
+    res = run(w, q, k, v, lens, max_len=128)
+    assert res["plan"].max_band == 128 and res["plan"].granule > 1
+    check(res, oracle_ref(w, q, k, v, lens), what=f"d{hs} lens beyond max_len")
+
+
 CLUSTER_CASES = [
     W("cl_mqa", 2, 16, 1, 512, 700, 0, lens=(700, 3), seed=61),
     W("cl_ring", 1, 16, 8, 256, 256, 200, lens=(1234,), seed=62),
