@@ -15,7 +15,9 @@ fixed 32 MiB array compiled into libfd.so. This file checks that:
     process, stay exact (no counter left non-zero between calls);
   * the first call of a fresh process, made on a non-blocking stream, is exact
     (the array's one-time clear is ordered before that call's kernels);
-  * a shape too large for the array is refused before anything runs.
+  * a shape too large for the array is refused before anything runs;
+  * after fd_release, the library-owned workspace and the array are set up
+    again on the next call, and both entry points stay exact.
 
 The file is collected last and depends on no other test: it passes alone in a
 fresh process and after the rest of the suite.
@@ -189,3 +191,24 @@ def test_noalloc_refuses_a_shape_beyond_its_scratch():
     assert "32 MiB" in fd.fd_strerror(rc)
     torch.cuda.synchronize()
     assert (out == 7.0).all()
+
+
+def test_release_re_arms_both_library_owned_paths():
+    """fd_release frees the library-owned workspaces and forgets the fixed
+    array's set-up (the recovery step after a failed call): the next
+    fd_decode_attn and fd_decode_attn_noalloc calls set up again - the array
+    is cleared again on the caller's stream - and both return exactly what
+    fd_decode_attn_ex returns."""
+    w = CASES[0]
+    lib = fd.load_library()
+    q, k, v, lens = _on_device(w, w.seed + 50)
+    ref = _explicit(w, q, k, v, lens)
+    for i in range(3):
+        got_na = _noalloc(lib, w, q, k, v, lens)
+        got_lib = torch.full_like(q, float("nan"))
+        fd.fd_decode_attn(q, k, v, got_lib, lens, w.B, w.NH, w.NKV, w.HS, w.capacity, w.window, w.scale)
+        torch.cuda.synchronize()
+        _assert_same(got_na, ref, f"noalloc, pass {i}")
+        _assert_same(got_lib, ref, f"library workspace, pass {i}")
+        fd.fd_release()
+    assert fd.fd_get_device_error() == 0
