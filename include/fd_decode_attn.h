@@ -385,8 +385,8 @@ int fd_decode_attn_fp8_ex(const fd_plan_t* plan, void* workspace, size_t workspa
  *     advance).
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress), clears the array with cudaMemsetAsync on
- *     `stream`, waits for `stream` (once), and caches the address; make that
- *     first call before any stream capture.
+ *     `stream`, waits for `stream` (once, so the clear has finished before any
+ *     call on any stream runs), and caches the address.
  *   - All calls on a device share the one array and each finds the previous
  *     call's contents in it. The counters must start at zero: the device's
  *     set-up clears the array once and every completed call leaves them zero.
